@@ -1,0 +1,347 @@
+"""Throughput of speculative-decoding verification on GB300.
+
+One step = the whole hot path over one batch: the tree-attention mask, the vocabulary-streaming
+row statistics over every (request, node) row, the per-request walk with rejection sampling,
+the inverse-CDF bonus draw and the accepted-path compaction, on the large-tree workload
+(B=256 requests, N=64-node random tries, V=152064 bf16 logits, temperature 1.0, point-mass
+drafts, supplied uniforms). Inputs are synthetic and seeded.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank verifies its own batch (requests are independent: weak scaling, no
+collective on the data path); the time is the max over ranks and rank 0 prints one JSON line.
+``--impl reference`` times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_mask_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verified draft nodes/s and logit-read GB/s (% of HBM peak), B=256 N=64 V=152064"
+UNIT = "draft nodes/s"
+WORKLOAD = "large_tree"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def config_of(w: W.Workload, world: int) -> dict:
+    return {"workload": f"{w.name}: B={w.B} N={w.N} V={w.V} {w.dtype} T={w.temperature} "
+                        f"point-mass drafts, random tries depth<={w.max_depth} "
+                        f"branching 1-{w.max_branch}",
+            "global_batch": w.B * world, "nodes_per_request": w.N, "vocab": w.V,
+            "parallelism": f"independent requests x{world}",
+            "l2": "inputs larger than L2 (logits %.2f GB per step)" % (w.B * w.N * w.V * 2 / 1e9)}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def traffic_record(kernel_file: str):
+    """Per-launch DRAM bytes of the row-stats kernel from the committed ncu summary, if the
+    kernel source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "speculative_decoding_tree_mask_gb300", "csrc", kernel_file)
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_file)
+    if not rec:
+        return None
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if rec.get("source_sha") == sha else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_oracle_sample(x, w, nthreads: int, reps_target_s: float = 10.0, max_reps: int = 5):
+    from oracle import oracle as O
+    orc = O.default()
+    logits = W.host_logits(x["logits"])
+    u = x["uniforms"].cpu().numpy()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        orc.verify_sample(logits, x["tok_np"], x["parent_np"], w.temperature, u,
+                          nthreads=nthreads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= reps_target_s or reps >= max_reps:
+            break
+    return reps * w.draft_nodes / el, reps, el
+
+
+def bench_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    w = W.WORKLOADS[WORKLOAD]
+    dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
+    x = W.make(w, device=dev)
+    from oracle import oracle as O
+    orc = O.default()
+    nthreads = os.cpu_count() or 1
+    logits = W.host_logits(x["logits"])
+    u = x["uniforms"].cpu().numpy()
+    del x["logits"]
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        orc.verify_sample(logits, x["tok_np"], x["parent_np"], w.temperature, u,
+                          nthreads=nthreads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = w.draft_nodes / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                             "sample": f"the whole {WORKLOAD} batch per step "
+                                       f"({w.B} requests), float64 C oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args):
+    from speculative_decoding_tree_mask_gb300 import binding as G
+
+    rank, world, local = dist_env()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    w = W.WORKLOADS[WORKLOAD]
+    x = W.make(w, device=dev, seed=w.seed + rank)
+    B, N, V, T = w.B, w.N, w.V, w.temperature
+    h = G.Handle(B, N, V, local)
+    mask = dict(anc_mask=torch.empty((B, N), dtype=torch.int64, device=dev),
+                depth=torch.empty((B, N), dtype=torch.int32, device=dev),
+                status=torch.empty(B, dtype=torch.int32, device=dev))
+    out = G.alloc_outputs(B, N, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        G.spec_build_tree_mask(h, x["parent"], mask["anc_mask"], mask["depth"], mask["status"],
+                               stream)
+        G.spec_verify_sample(h, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"],
+                             out["accept_len"], out["out_tokens"], out["kv_commit"],
+                             out["bonus"], out["status"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        G.spec_profile_begin(h)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        prof = G.spec_profile_end(h)
+    barrier(world)
+    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms, world, dev)
+    value = world * w.draft_nodes / (ms / 1e3)
+
+    # dominant kernel: row statistics over all B*N rows
+    rs_ms, rs_n = prof["row_stats"]
+    rs_avg = rs_ms / max(rs_n, 1)
+    alg_bytes = B * N * V * w.elem_bytes
+    pk, pk_kind = peaks()
+    achieved = alg_bytes / (rs_avg / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic_record("row_stats.cu"),
+                "kernel": "row_stats_kernel<bf16, sample>", "peak_source": pk_kind,
+                "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": rs_avg}
+    step_bytes = alg_bytes  # logits read once per step (bonus row and metadata excluded)
+    kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
+               for k, v in prof.items() if v[1]}
+
+    # end to end: pinned host inputs -> device, verify, outputs -> pinned host, every step
+    e2e = None
+    if not args.skip_e2e:
+        hl = torch.empty_like(x["logits"], device="cpu").pin_memory()
+        hl.copy_(x["logits"])
+        hsmall = {k: x[k].cpu().pin_memory() for k in ("draft_token", "parent", "uniforms")}
+        hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in out.items()}
+        hmask = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in mask.items()}
+        h2d = hl.numel() * hl.element_size() + sum(t.numel() * t.element_size()
+                                                   for t in hsmall.values())
+        d2h = sum(t.numel() * t.element_size() for t in list(hout.values()) +
+                  list(hmask.values()))
+
+        def e2e_step():
+            x["logits"].copy_(hl, non_blocking=True)
+            for k, t in hsmall.items():
+                x[k].copy_(t, non_blocking=True)
+            step()
+            for k, t in hout.items():
+                t.copy_(out[k], non_blocking=True)
+            for k, t in hmask.items():
+                t.copy_(mask[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        k2 = args.e2e_steps
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        t2.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = max_over_ranks(s2.elapsed_time(t2) / k2, world, dev)
+        e2e = {"value": world * w.draft_nodes / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": ems, "steps": k2}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        cval, reps, el = run_oracle_sample(x, w, nthreads)
+        cpu = {"value": cval, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+               "sample": f"the whole {WORKLOAD} batch ({w.B} requests) x{reps} "
+                         f"({el:.1f} s), float64 C oracle, OpenMP over requests"}
+
+    hist = np.bincount(out["accept_len"].cpu().numpy(), minlength=1).tolist()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded random tries and N(0,3) logits)",
+                "config": config_of(w, world),
+                "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
+                "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * args.steps, "kernels": kernels,
+                "clocks": clocks.summary(), "accept_len_hist": hist}
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

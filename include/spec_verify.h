@@ -1,0 +1,180 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding verification library.
+ *
+ * The operation (EmbodiInfer PR #11 "perf(activevln): grammar-trie speculation and lossless
+ * throughput", commit 4b728e2 "grammar-trie tree speculation with exact acceptance"): the
+ * draft is a trie of N nodes (node 0 is the root, the last committed token) whose logits the
+ * target model produced in one tree-attention forward, one row per node. Verification turns
+ * those rows into an exact accept/reject decision per request: greedy decoding keeps the
+ * argmax path, sampling uses standard (SpecInfer-style) rejection sampling against the draft
+ * so the output distribution equals the target's, and a bonus token is drawn where the walk
+ * stops. IluvatarLabs/vllm PR #3 "SCV vectorized masking" computes the per-request
+ * acceptance mask on the device without host synchronisation; this library likewise never
+ * synchronises with the host inside a call.
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers owned by the caller, row-major and contiguous.
+ *     They must be aligned to their element size. Logits rows have stride V elements.
+ *   - Tree: parent int32 [B, N] with parent[b][0] == -1 and 0 <= parent[b][i] < i
+ *     (topological order); draft_token int32 [B, N], entry 0 (the root) is ignored. Children
+ *     of a node are visited in ascending node index ("trie order"). 1 <= N <= 64.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     never synchronise the host. One handle serves one stream at a time (its workspace is
+ *     reused by every call).
+ *   - Host-checkable problems (NULL handle or pointer, sizes beyond the handle's limits,
+ *     unknown dtype, bad temperature) return a negative SPEC_ERR_* code synchronously and
+ *     launch nothing. Problems in the data are reported per request in status[b]
+ *     (SPEC_REQ_*); a request with nonzero status gets accept_len 0, bonus -1 and -1 in
+ *     every out_tokens / kv_commit slot. SPEC_ERR_CUDA means a launch failed.
+ *   - Outputs of a verify call, per request b:
+ *       accept_len[b]          number of accepted non-root nodes L;
+ *       out_tokens[b][0..L]    draft tokens of the accepted nodes in path order, then the
+ *                              bonus token; -1 beyond L;
+ *       kv_commit[b][0..L]     node ids whose KV entries to keep: 0 (the root, produced by
+ *                              the same forward) then the accepted nodes; -1 beyond L;
+ *       bonus[b]               the bonus token;  status[b]  SPEC_REQ_*.
+ *     out_tokens and kv_commit are int32 [B, N].
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_ctx *spec_handle;
+
+enum {
+    SPEC_OK = 0,
+    SPEC_ERR_ARG = -1,          /* an argument is invalid or outside the handle's limits */
+    SPEC_ERR_UNSUPPORTED = -2,  /* a valid request this build does not implement */
+    SPEC_ERR_CUDA = -3,         /* a CUDA call or launch failed */
+    SPEC_ERR_WORKSPACE = -4     /* workspace allocation failed */
+};
+
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };  /* element type of logits / draft logits */
+
+enum {
+    SPEC_DRAFT_POINT = 0,       /* deterministic trie: the draft puts mass 1 on each child */
+    SPEC_DRAFT_PROBS_F32 = 1,   /* draft probabilities float32 [B, N, V], used as given */
+    SPEC_DRAFT_LOGITS = 2       /* draft logits [B, N, V] (SPEC_F32 / SPEC_BF16), softmax(d/T) */
+};
+
+enum {
+    SPEC_REQ_OK = 0,
+    SPEC_REQ_BAD_PARENT = 1,    /* parent[0] != -1 or parent[i] outside [0, i) */
+    SPEC_REQ_BAD_TOKEN = 2,     /* a non-root draft token outside [0, V) */
+    SPEC_REQ_BAD_ROW = 3,       /* a row the walk needs holds NaN / +inf or is all -inf
+                                   (for probabilities: NaN, inf or a negative entry) */
+    SPEC_REQ_BAD_UNIFORM = 4    /* a uniform in slots 1..N is NaN or outside [0, 1) */
+};
+
+/* Row-statistics flag bits (spec_row_stats row_flags). */
+enum { SPEC_ROW_NAN = 1, SPEC_ROW_POSINF = 2, SPEC_ROW_ALL_NEGINF = 4 };
+
+/* Kernel classes reported by the profiling calls. */
+enum {
+    SPEC_K_TREE_MASK = 0,
+    SPEC_K_ROW_STATS = 1,       /* target logits rows */
+    SPEC_K_DRAFT_STATS = 2,     /* dense draft rows */
+    SPEC_K_WALK_GREEDY = 3,
+    SPEC_K_WALK_SAMPLE = 4,
+    SPEC_K_COUNT = 5
+};
+
+/*
+ * Create a handle for `device` able to serve calls with B <= max_B, N <= max_N (<= 64) and
+ * V <= max_V (<= 2^21). Allocates a device workspace of 36 * max_B * max_N bytes with
+ * cudaMalloc (released by spec_verify_destroy). Returns SPEC_ERR_ARG for out-of-range limits,
+ * SPEC_ERR_CUDA if the device cannot be used, SPEC_ERR_WORKSPACE if allocation fails.
+ */
+int spec_verify_init(spec_handle *h, int max_B, int max_N, int64_t max_V, int device);
+
+/* Free the handle and its workspace. Waits for nothing: the caller must ensure no call on
+ * the handle is still running. NULL is accepted. */
+int spec_verify_destroy(spec_handle h);
+
+/*
+ * Tree-attention mask (EmbodiInfer PR #11, commit 4b728e2: all N nodes are verified in one
+ * tree-attention forward; IluvatarLabs/vllm PR #3: the mask is built on the device).
+ * anc_mask uint64 [B, N]: bit j of anc_mask[b][i] is set iff node j is node i or one of its
+ * ancestors, i.e. query i may attend to key j. depth int32 [B, N]: number of edges from the
+ * root. status int32 [B]: SPEC_REQ_OK or SPEC_REQ_BAD_PARENT (then the request's masks are 0
+ * and depths -1).
+ */
+int spec_build_tree_mask(spec_handle h, const int32_t *parent, int B, int N, uint64_t *anc_mask,
+                         int32_t *depth, int32_t *status, void *stream);
+
+/*
+ * Greedy verification (EmbodiInfer PR #11, commit 4b728e2: greedy keeps the argmax path).
+ * logits [B, N, V] of `dtype` (SPEC_F32 / SPEC_BF16). From the root, repeatedly take
+ * a = argmax of the current node's row (lowest index on ties) and move to the first child in
+ * trie order whose draft token equals a; stop when none does. The bonus is a at the stop
+ * node. Rows of nodes off the path never influence an output (NaN there is harmless).
+ */
+int spec_verify_greedy(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                       const int32_t *draft_token, const int32_t *parent, int32_t *accept_len,
+                       int32_t *out_tokens, int32_t *kv_commit, int32_t *bonus, int32_t *status,
+                       void *stream);
+
+/*
+ * Sampling verification (EmbodiInfer PR #11, commit 4b728e2: standard rejection sampling
+ * against the draft, output distribution unchanged). p = softmax(z / temperature) per row;
+ * temperature == 0 runs spec_verify_greedy (the draft and uniforms are then ignored);
+ * temperature must be finite and >= 0.
+ * uniforms float32 [B, N+1] in [0, 1): slot c is consumed when child c is tested, slot N
+ * draws the bonus, slot 0 is unused.
+ *   SPEC_DRAFT_POINT (draft NULL): at a node with rejected-token set R, child c with token t
+ *     is accepted iff u[c] < p(t) / sum_{v not in R} p(v) (0 if t is in R); on rejection t
+ *     joins R; when the walk stops the bonus is the inverse CDF of p with R zeroed at u[N].
+ *   SPEC_DRAFT_PROBS_F32 / SPEC_DRAFT_LOGITS: draft row i is the distribution q that drafted
+ *     node i's children (the same temperature is applied to draft logits). Child c with
+ *     token x is accepted iff u[c] * q(x) < r(x), r starting as p; on rejection
+ *     r <- max(r - q, 0) / sum(max(r - q, 0)) (kept unchanged if that sum is 0); the bonus is
+ *     the inverse CDF of r at u[N] (of p at a leaf). On a chain this is standard speculative
+ *     sampling; on a tree, siblings are taken as independent draws from q.
+ * Inverse CDF: with S = sum r and tau = u*S, the smallest v whose running sum exceeds tau
+ * (the largest v with r(v) > 0 if rounding leaves none).
+ */
+int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                       const int32_t *draft_token, const int32_t *parent, const void *draft,
+                       int draft_kind, int draft_dtype, float temperature,
+                       const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
+                       int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream);
+
+/*
+ * The vocabulary-streaming row statistics on their own (the first stage of both verify
+ * calls), for `rows` contiguous rows of V elements:
+ *   row_max[r]    max_v z[r][v] (float32; exact for bf16/f32 inputs)
+ *   row_argmax[r] lowest index attaining it
+ *   row_sum[r]    sum_v exp((z[r][v] - row_max[r]) / temperature), or 0 when temperature == 0
+ *   row_flags[r]  SPEC_ROW_* bits (nonzero = the row is unusable for verification)
+ * If draft_token, parent and child_prob are all non-NULL the rows are read as [B, N, V]
+ * with B = rows / N, and child_prob[b][c] = p_{parent(c)}(draft_token[b][c]) for every
+ * non-root node c whose parent is in range and whose token is in [0, V) (other slots are
+ * left untouched); temperature must then be > 0.
+ */
+int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N, int64_t V,
+                   float temperature, const int32_t *draft_token, const int32_t *parent,
+                   float *row_max, float *row_sum, int32_t *row_argmax, int32_t *row_flags,
+                   float *child_prob, void *stream);
+
+/*
+ * Per-kernel timing. After spec_profile_begin, every kernel launched through the handle is
+ * bracketed with CUDA events on its stream (at most 16384 launches are recorded).
+ * spec_profile_end waits for those events and writes, per SPEC_K_* class, the summed
+ * device milliseconds and the number of launches, then stops recording.
+ */
+int spec_profile_begin(spec_handle h);
+int spec_profile_end(spec_handle h, float *ms_per_class, int32_t *launches_per_class);
+
+/* Static description of a SPEC_ERR_* code. */
+const char *spec_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

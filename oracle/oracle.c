@@ -391,7 +391,8 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
             if (par[c] != node) continue;
             int32_t x = tok[c];
             double lhs = (double)u[c] * q[x];
-            double mg = fabs(lhs - r[x]);
+            /* decision margin in normalised terms: the test is u < r(x)/q(x) */
+            double mg = q[x] > 0.0 ? fabs(lhs - r[x]) / q[x] : r[x];
             if (mg < *dmargin) *dmargin = mg;
             if (lhs < r[x]) {
                 next = c;
@@ -424,9 +425,10 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
 
 /* Sampling verify. T == 0 is greedy. Uniforms have shape [B, N+1]; every slot 1..N must lie
  * in [0, 1) or the request fails with status 4 (READING: checked before the walk, whether or
- * not the walk consumes the slot). decision_margin[b] is the smallest |u*q - r| over the
- * tests taken (+inf if none), cdf_margin[b] the bonus draw's margin, degenerate[b] the
- * number of degenerate dense residuals. */
+ * not the walk consumes the slot). decision_margin[b] is the smallest |u - r(x)/q(x)| over
+ * the tests taken (= |u*q - r|/q, never below |u*q - r| as q <= 1; +inf if no test),
+ * cdf_margin[b] the bonus draw's margin, degenerate[b] the number of degenerate dense
+ * residuals. */
 int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
                          const int32_t *draft_token, const int32_t *parent, const void *draft,
                          int draft_kind, int draft_dtype, double T, const float *uniforms,

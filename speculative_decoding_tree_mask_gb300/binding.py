@@ -1,0 +1,235 @@
+"""ctypes binding of ``libspecverify.so`` (C ABI in ``include/spec_verify.h``).
+
+Argument marshalling only: every step runs in the library's CUDA kernels. Tensors are torch
+CUDA tensors (torch provides device memory and streams); the functions keep the C names.
+Loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libspecverify.so")
+
+SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE = 0, -1, -2, -3, -4
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_DRAFT_POINT, SPEC_DRAFT_PROBS_F32, SPEC_DRAFT_LOGITS = 0, 1, 2
+SPEC_REQ_OK, SPEC_REQ_BAD_PARENT, SPEC_REQ_BAD_TOKEN, SPEC_REQ_BAD_ROW, SPEC_REQ_BAD_UNIFORM = \
+    0, 1, 2, 3, 4
+SPEC_ROW_NAN, SPEC_ROW_POSINF, SPEC_ROW_ALL_NEGINF = 1, 2, 4
+KERNEL_CLASSES = ("tree_mask", "row_stats", "draft_stats", "walk_greedy", "walk_sample")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} ({code})")
+
+
+def load() -> ctypes.CDLL:
+    """Open the CUDA library (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(
+                    f"{LIBRARY} is missing: build it first "
+                    "(python -m speculative_decoding_tree_mask_gb300.build)")
+            lib = ctypes.CDLL(LIBRARY)
+            P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+            lib.spec_verify_init.argtypes = [ctypes.POINTER(P), i32, i32, i64, i32]
+            lib.spec_verify_destroy.argtypes = [P]
+            lib.spec_build_tree_mask.argtypes = [P, P, i32, i32, P, P, P, P]
+            lib.spec_verify_greedy.argtypes = [P, P, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+            lib.spec_verify_sample.argtypes = [P, P, i32, i32, i32, i64, P, P, P, i32, i32, f32,
+                                               P, P, P, P, P, P, P]
+            lib.spec_row_stats.argtypes = [P, P, i32, i32, i32, i64, f32, P, P, P, P, P, P, P, P]
+            lib.spec_profile_begin.argtypes = [P]
+            lib.spec_profile_end.argtypes = [P, P, P]
+            lib.spec_error_string.argtypes = [i32]
+            lib.spec_error_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return load().spec_error_string(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != SPEC_OK:
+        raise SpecError(rc, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return t
+
+
+class Handle:
+    """Owner of a ``spec_handle`` (workspace for B <= max_B, N <= max_N, V <= max_V)."""
+
+    def __init__(self, max_B: int, max_N: int, max_V: int, device: int = 0):
+        h = ctypes.c_void_p()
+        _check(load().spec_verify_init(ctypes.byref(h), int(max_B), int(max_N), int(max_V),
+                                       int(device)), "spec_verify_init")
+        self.ptr = h
+        self.device = int(device)
+        self.max_B, self.max_N, self.max_V = int(max_B), int(max_N), int(max_V)
+
+    def close(self):
+        if self.ptr is not None and self.ptr.value:
+            load().spec_verify_destroy(self.ptr)
+        self.ptr = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spec_verify_init(max_B: int, max_N: int, max_V: int, device: int = 0) -> Handle:
+    return Handle(max_B, max_N, max_V, device)
+
+
+def spec_verify_destroy(h: Handle):
+    h.close()
+
+
+def spec_build_tree_mask(h: Handle, parent, anc_mask, depth, status, stream=None):
+    """parent int32 [B, N] -> anc_mask int64 [B, N] (uint64 bit patterns), depth int32 [B, N],
+    status int32 [B]."""
+    B, N = parent.shape
+    if anc_mask.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)):
+        raise TypeError("anc_mask must be a 64-bit integer tensor")
+    _check(load().spec_build_tree_mask(h.ptr, _ptr(_i32(parent, "parent")), B, N, _ptr(anc_mask),
+                                       _ptr(_i32(depth, "depth")), _ptr(_i32(status, "status")),
+                                       _stream(stream, parent.device)), "spec_build_tree_mask")
+
+
+def spec_verify_greedy(h: Handle, logits, draft_token, parent, accept_len, out_tokens, kv_commit,
+                       bonus, status, stream=None):
+    B, N, V = logits.shape
+    _check(load().spec_verify_greedy(
+        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
+        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
+        _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
+        _stream(stream, logits.device)), "spec_verify_greedy")
+
+
+def spec_verify_sample(h: Handle, logits, draft_token, parent, temperature: float, uniforms,
+                       accept_len, out_tokens, kv_commit, bonus, status, draft=None,
+                       draft_kind: int = SPEC_DRAFT_POINT, stream=None):
+    B, N, V = logits.shape
+    ddt = 0
+    if draft is not None and draft_kind == SPEC_DRAFT_LOGITS:
+        ddt = _dtype_code(draft)
+    if draft is not None and draft_kind == SPEC_DRAFT_PROBS_F32 and draft.dtype != torch.float32:
+        raise TypeError("draft probabilities must be float32")
+    _check(load().spec_verify_sample(
+        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
+        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")), _ptr(draft),
+        int(draft_kind), ddt, float(temperature), _ptr(uniforms), _ptr(accept_len),
+        _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
+        _stream(stream, logits.device)), "spec_verify_sample")
+
+
+def spec_row_stats(h: Handle, logits, N: int, temperature: float, row_max, row_sum, row_argmax,
+                   row_flags, draft_token=None, parent=None, child_prob=None, stream=None):
+    """logits [rows, V] (or [B, N, V]) -> per-row max, sum, argmax, flags; optional gather of
+    p_parent(token) at every child into child_prob [B, N]."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    _check(load().spec_row_stats(
+        h.ptr, _ptr(logits), _dtype_code(logits), rows, int(N), V, float(temperature),
+        _ptr(draft_token), _ptr(parent), _ptr(row_max), _ptr(row_sum), _ptr(row_argmax),
+        _ptr(row_flags), _ptr(child_prob), _stream(stream, logits.device)), "spec_row_stats")
+
+
+def spec_profile_begin(h: Handle):
+    _check(load().spec_profile_begin(h.ptr), "spec_profile_begin")
+
+
+def spec_profile_end(h: Handle):
+    """-> {kernel class: (total ms, launches)} for the launches since spec_profile_begin."""
+    ms = (ctypes.c_float * len(KERNEL_CLASSES))()
+    n = (ctypes.c_int32 * len(KERNEL_CLASSES))()
+    _check(load().spec_profile_end(h.ptr, ms, n), "spec_profile_end")
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+# ---- convenience: allocate outputs -----------------------------------------------------------
+
+def alloc_outputs(B: int, N: int, device) -> dict:
+    opts = dict(dtype=torch.int32, device=device)
+    return dict(accept_len=torch.empty(B, **opts), out_tokens=torch.empty((B, N), **opts),
+                kv_commit=torch.empty((B, N), **opts), bonus=torch.empty(B, **opts),
+                status=torch.empty(B, **opts))
+
+
+def verify_greedy(h: Handle, logits, draft_token, parent, out: dict | None = None,
+                  stream=None) -> dict:
+    B, N, _ = logits.shape
+    out = out or alloc_outputs(B, N, logits.device)
+    spec_verify_greedy(h, logits, draft_token, parent, out["accept_len"], out["out_tokens"],
+                       out["kv_commit"], out["bonus"], out["status"], stream)
+    return out
+
+
+def verify_sample(h: Handle, logits, draft_token, parent, temperature, uniforms, draft=None,
+                  draft_kind=SPEC_DRAFT_POINT, out: dict | None = None, stream=None) -> dict:
+    B, N, _ = logits.shape
+    out = out or alloc_outputs(B, N, logits.device)
+    spec_verify_sample(h, logits, draft_token, parent, temperature, uniforms, out["accept_len"],
+                       out["out_tokens"], out["kv_commit"], out["bonus"], out["status"], draft,
+                       draft_kind, stream)
+    return out
+
+
+def build_tree_mask(h: Handle, parent, stream=None) -> dict:
+    B, N = parent.shape
+    dev = parent.device
+    out = dict(anc_mask=torch.empty((B, N), dtype=torch.int64, device=dev),
+               depth=torch.empty((B, N), dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    spec_build_tree_mask(h, parent, out["anc_mask"], out["depth"], out["status"], stream)
+    return out

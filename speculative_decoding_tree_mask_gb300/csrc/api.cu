@@ -1,0 +1,399 @@
+// C ABI of the verification library (declared in include/spec_verify.h): handle and
+// workspace, host-side argument checks, kernel orchestration and per-kernel timing.
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+
+#include "spec_internal.h"
+#include "spec_verify.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kMaxRecords = 16384;
+constexpr int64_t kMaxV = int64_t(1) << 21;
+constexpr float kLog2eF = 1.4426950408889634f;
+
+}  // namespace
+
+struct spec_ctx {
+    int device = 0;
+    int max_B = 0, max_N = 0;
+    int64_t max_V = 0;
+    void *ws = nullptr;
+    float *m = nullptr, *s = nullptr, *pc = nullptr, *mq = nullptr, *sq = nullptr,
+          *qc = nullptr;
+    int32_t *arg = nullptr, *flags = nullptr, *dflags = nullptr;
+    bool prof = false;
+    bool ev_ready = false;
+    int nrec = 0;
+    cudaEvent_t ev[2 * kMaxRecords];
+    int cls[kMaxRecords];
+};
+
+namespace {
+
+// Makes the handle's device current for the duration of a call and restores the caller's.
+class DeviceScope {
+  public:
+    explicit DeviceScope(int dev) {
+        ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+        if (ok_ && prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+        switched_ = ok_ && prev_ != dev;
+    }
+    ~DeviceScope() {
+        if (switched_) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+  private:
+    int prev_ = 0;
+    bool ok_ = false, switched_ = false;
+};
+
+template <typename F>
+int timed(spec_handle h, int cls, cudaStream_t st, F &&launch) {
+    int slot = -1;
+    if (h->prof && h->nrec < kMaxRecords) {
+        slot = h->nrec++;
+        h->cls[slot] = cls;
+        cudaEventRecord(h->ev[2 * slot], st);
+    }
+    const cudaError_t e = launch();
+    if (slot >= 0) cudaEventRecord(h->ev[2 * slot + 1], st);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+int check_common(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                 const int32_t *tok, const int32_t *parent, const int32_t *accept_len,
+                 const int32_t *out_tokens, const int32_t *kv_commit, const int32_t *bonus,
+                 const int32_t *status) {
+    if (!h) return SPEC_ERR_ARG;
+    if (B < 0 || B > h->max_B) return SPEC_ERR_ARG;
+    if (N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
+    if (V < 1 || V > h->max_V) return SPEC_ERR_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!logits || !tok || !parent || !accept_len || !out_tokens || !kv_commit || !bonus ||
+        !status)
+        return SPEC_ERR_ARG;
+    if (!aligned(logits, esize(dtype))) return SPEC_ERR_ARG;
+    const void *ints[] = {tok, parent, accept_len, out_tokens, kv_commit, bonus, status};
+    for (const void *p : ints)
+        if (!aligned(p, 4)) return SPEC_ERR_ARG;
+    return SPEC_OK;
+}
+
+WalkOutputs outputs(int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
+                    int32_t *bonus, int32_t *status) {
+    WalkOutputs o;
+    o.accept_len = accept_len;
+    o.out_tokens = out_tokens;
+    o.kv_commit = kv_commit;
+    o.bonus = bonus;
+    o.status = status;
+    return o;
+}
+
+int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                const int32_t *tok, const int32_t *parent, WalkOutputs out, cudaStream_t st) {
+    RowStatsParams rp{};
+    rp.x = logits;
+    rp.V = V;
+    rp.rows = B * N;
+    rp.N = N;
+    rp.k = 0.f;
+    rp.m = h->m;
+    rp.s = nullptr;
+    rp.arg = h->arg;
+    rp.flags = h->flags;
+    int rc = timed(h, SPEC_K_ROW_STATS, st,
+                   [&] { return launch_row_stats(rp, dtype, ROW_GREEDY, st); });
+    if (rc != SPEC_OK) return rc;
+    GreedyWalkParams gp;
+    gp.B = B;
+    gp.N = N;
+    gp.V = V;
+    gp.parent = parent;
+    gp.tok = tok;
+    gp.arg = h->arg;
+    gp.flags = h->flags;
+    gp.out = out;
+    return timed(h, SPEC_K_WALK_GREEDY, st, [&] { return launch_walk_greedy(gp, st); });
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *spec_error_string(int code) {
+    switch (code) {
+        case SPEC_OK: return "ok";
+        case SPEC_ERR_ARG: return "invalid argument or outside the handle's limits";
+        case SPEC_ERR_UNSUPPORTED: return "unsupported request";
+        case SPEC_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case SPEC_ERR_WORKSPACE: return "workspace allocation failed";
+        default: return "unknown error code";
+    }
+}
+
+int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int device) {
+    if (!out) return SPEC_ERR_ARG;
+    *out = nullptr;
+    if (max_B < 1 || max_N < 1 || max_V < 1) return SPEC_ERR_ARG;
+    if (max_N > kMaxN || max_V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+    if ((int64_t)max_B * max_N > (int64_t(1) << 30)) return SPEC_ERR_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return SPEC_ERR_CUDA;
+    DeviceScope ds(device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    spec_ctx *h = new (std::nothrow) spec_ctx();
+    if (!h) return SPEC_ERR_WORKSPACE;
+    h->device = device;
+    h->max_B = max_B;
+    h->max_N = max_N;
+    h->max_V = max_V;
+    const size_t rows = (size_t)max_B * max_N;
+    const size_t bytes = rows * 9 * 4;
+    if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return SPEC_ERR_WORKSPACE;
+    }
+    char *p = static_cast<char *>(h->ws);
+    auto take = [&](size_t n) {
+        char *q = p;
+        p += n;
+        return q;
+    };
+    h->m = reinterpret_cast<float *>(take(rows * 4));
+    h->s = reinterpret_cast<float *>(take(rows * 4));
+    h->pc = reinterpret_cast<float *>(take(rows * 4));
+    h->mq = reinterpret_cast<float *>(take(rows * 4));
+    h->sq = reinterpret_cast<float *>(take(rows * 4));
+    h->qc = reinterpret_cast<float *>(take(rows * 4));
+    h->arg = reinterpret_cast<int32_t *>(take(rows * 4));
+    h->flags = reinterpret_cast<int32_t *>(take(rows * 4));
+    h->dflags = reinterpret_cast<int32_t *>(take(rows * 4));
+    *out = h;
+    return SPEC_OK;
+}
+
+int spec_verify_destroy(spec_handle h) {
+    if (!h) return SPEC_OK;
+    DeviceScope ds(h->device);
+    if (h->ev_ready)
+        for (int i = 0; i < 2 * kMaxRecords; ++i) cudaEventDestroy(h->ev[i]);
+    cudaFree(h->ws);
+    delete h;
+    return SPEC_OK;
+}
+
+int spec_build_tree_mask(spec_handle h, const int32_t *parent, int B, int N, uint64_t *anc_mask,
+                         int32_t *depth, int32_t *status, void *stream) {
+    if (!h) return SPEC_ERR_ARG;
+    if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!parent || !anc_mask || !depth || !status) return SPEC_ERR_ARG;
+    if (!aligned(parent, 4) || !aligned(anc_mask, 8) || !aligned(depth, 4) || !aligned(status, 4))
+        return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return timed(h, SPEC_K_TREE_MASK, st, [&] {
+        return launch_tree_mask(parent, B, N, anc_mask, depth, status, st);
+    });
+}
+
+int spec_verify_greedy(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                       const int32_t *draft_token, const int32_t *parent, int32_t *accept_len,
+                       int32_t *out_tokens, int32_t *kv_commit, int32_t *bonus, int32_t *status,
+                       void *stream) {
+    int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
+                          out_tokens, kv_commit, bonus, status);
+    if (rc != SPEC_OK || B == 0) return rc;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    return greedy_impl(h, logits, dtype, B, N, V, draft_token, parent,
+                       outputs(accept_len, out_tokens, kv_commit, bonus, status),
+                       static_cast<cudaStream_t>(stream));
+}
+
+int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
+                       const int32_t *draft_token, const int32_t *parent, const void *draft,
+                       int draft_kind, int draft_dtype, float temperature,
+                       const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
+                       int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream) {
+    int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
+                          out_tokens, kv_commit, bonus, status);
+    if (rc != SPEC_OK) return rc;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return SPEC_ERR_ARG;
+    const float k = temperature > 0.f ? kLog2eF / temperature : 0.f;
+    if (temperature > 0.f && !std::isfinite(k)) return SPEC_ERR_ARG;
+    if (draft_kind != SPEC_DRAFT_POINT && draft_kind != SPEC_DRAFT_PROBS_F32 &&
+        draft_kind != SPEC_DRAFT_LOGITS)
+        return SPEC_ERR_ARG;
+    if (draft_kind == SPEC_DRAFT_LOGITS && draft_dtype != SPEC_F32 && draft_dtype != SPEC_BF16)
+        return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WalkOutputs out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
+    if (temperature == 0.f)
+        return greedy_impl(h, logits, dtype, B, N, V, draft_token, parent, out, st);
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_ARG;
+    const bool dense = draft_kind != SPEC_DRAFT_POINT;
+    if (dense) {
+        if (!draft) return SPEC_ERR_ARG;
+        const size_t de = draft_kind == SPEC_DRAFT_LOGITS ? esize(draft_dtype) : 4;
+        if (!aligned(draft, de)) return SPEC_ERR_ARG;
+    }
+
+    RowStatsParams rp{};
+    rp.x = logits;
+    rp.V = V;
+    rp.rows = B * N;
+    rp.N = N;
+    rp.k = k;
+    rp.parent = parent;
+    rp.tok = draft_token;
+    rp.skip_leaves = 0;
+    rp.pc_normalized = 0;
+    rp.m = h->m;
+    rp.s = h->s;
+    rp.arg = nullptr;
+    rp.flags = h->flags;
+    rp.pc = h->pc;
+    rc = timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
+    if (rc != SPEC_OK) return rc;
+
+    if (dense) {
+        RowStatsParams dp = rp;
+        dp.x = draft;
+        dp.skip_leaves = 1;
+        dp.flags = h->dflags;
+        dp.pc = h->qc;
+        int mode = ROW_PROBS, ddt = SPEC_F32;
+        if (draft_kind == SPEC_DRAFT_LOGITS) {
+            mode = ROW_SAMPLE;
+            ddt = draft_dtype;
+            dp.m = h->mq;
+            dp.s = h->sq;
+        } else {
+            dp.m = nullptr;
+            dp.s = nullptr;
+        }
+        rc = timed(h, SPEC_K_DRAFT_STATS, st, [&] { return launch_row_stats(dp, ddt, mode, st); });
+        if (rc != SPEC_OK) return rc;
+    }
+
+    SampleWalkParams wp{};
+    wp.B = B;
+    wp.N = N;
+    wp.V = V;
+    wp.dtype = dtype;
+    wp.logits = logits;
+    wp.parent = parent;
+    wp.tok = draft_token;
+    wp.uniforms = uniforms;
+    wp.k = k;
+    wp.m = h->m;
+    wp.s = h->s;
+    wp.pc = h->pc;
+    wp.flags = h->flags;
+    wp.draft_kind = draft_kind;
+    wp.draft_dtype = draft_dtype;
+    wp.draft = draft;
+    wp.mq = h->mq;
+    wp.sq = h->sq;
+    wp.qc = h->qc;
+    wp.dflags = h->dflags;
+    wp.out = out;
+    return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
+}
+
+int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N, int64_t V,
+                   float temperature, const int32_t *draft_token, const int32_t *parent,
+                   float *row_max, float *row_sum, int32_t *row_argmax, int32_t *row_flags,
+                   float *child_prob, void *stream) {
+    if (!h) return SPEC_ERR_ARG;
+    if (rows < 0 || N < 1 || N > kMaxN || V < 1 || V > kMaxV) return SPEC_ERR_ARG;
+    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_ARG;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return SPEC_ERR_ARG;
+    const float k = temperature > 0.f ? kLog2eF / temperature : 0.f;
+    if (temperature > 0.f && !std::isfinite(k)) return SPEC_ERR_ARG;
+    const bool gather = draft_token && parent && child_prob;
+    if (gather && (temperature == 0.f || rows % N != 0)) return SPEC_ERR_ARG;
+    if (rows == 0) return SPEC_OK;
+    if (!logits || !row_max || !row_sum || !row_argmax || !row_flags) return SPEC_ERR_ARG;
+    if (!aligned(logits, esize(dtype))) return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    RowStatsParams rp{};
+    rp.x = logits;
+    rp.V = V;
+    rp.rows = rows;
+    rp.N = N;
+    rp.k = k;
+    rp.parent = gather ? parent : nullptr;
+    rp.tok = gather ? draft_token : nullptr;
+    rp.skip_leaves = 0;
+    rp.pc_normalized = 1;
+    rp.m = row_max;
+    rp.s = row_sum;
+    rp.arg = row_argmax;
+    rp.flags = row_flags;
+    rp.pc = gather ? child_prob : nullptr;
+    const int mode = temperature > 0.f ? ROW_SAMPLE : ROW_GREEDY;
+    return timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, mode, st); });
+}
+
+int spec_profile_begin(spec_handle h) {
+    if (!h) return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    if (!h->ev_ready) {
+        for (int i = 0; i < 2 * kMaxRecords; ++i)
+            if (cudaEventCreate(&h->ev[i]) != cudaSuccess) return SPEC_ERR_CUDA;
+        h->ev_ready = true;
+    }
+    h->nrec = 0;
+    h->prof = true;
+    return SPEC_OK;
+}
+
+int spec_profile_end(spec_handle h, float *ms_per_class, int32_t *launches_per_class) {
+    if (!h || !ms_per_class || !launches_per_class) return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    for (int c = 0; c < SPEC_K_COUNT; ++c) {
+        ms_per_class[c] = 0.f;
+        launches_per_class[c] = 0;
+    }
+    int rc = SPEC_OK;
+    for (int i = 0; i < h->nrec; ++i) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(h->ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) != cudaSuccess) {
+            rc = SPEC_ERR_CUDA;
+            continue;
+        }
+        ms_per_class[h->cls[i]] += ms;
+        launches_per_class[h->cls[i]] += 1;
+    }
+    h->prof = false;
+    h->nrec = 0;
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+// Vocabulary-streaming row statistics: one CTA per (request, node) row.
+//
+// EmbodiInfer PR #11 "perf(activevln): grammar-trie speculation and lossless throughput"
+// (commit 4b728e2) verifies the N trie nodes in one forward, so every node has a logits row;
+// acceptance needs, per row, the argmax (greedy), and the softmax normaliser at temperature T
+// plus p at the drafted child tokens (rejection sampling). All of it comes out of one pass
+// over the row:
+//   m = max_v z_v, a = lowest index attaining m, S = sum_v 2^((z_v - m) * log2(e)/T),
+//   and p(child token) = 2^((z_t - m) * log2(e)/T) / S for every child of the row's node.
+// The running max is updated per 16-byte vector (8 bf16): a vector whose NaN-propagating max
+// does not exceed the running max costs 4 packed max instructions; otherwise (rare: O(log n)
+// times per thread) the sum is rescaled. Elements are visited in increasing index order per
+// thread, so a strict '>' keeps the lowest index; partial results merge lowest-index-first.
+// The stream is HBM-bound: 16-byte read-only loads, 4 in flight per thread, 512 threads.
+
+#include <cfloat>
+
+#include "spec_device.cuh"
+#include "spec_internal.h"
+
+namespace specv {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 4;
+
+enum { F_NAN = 1, F_POSINF = 2, F_ALLNEG = 4 };
+
+struct Acc {
+    float m;      // running max (never NaN)
+    float negm;   // -m once m is finite, else 0
+    float s0, s1; // partial sums of 2^((x - m) k)
+    int arg;      // lowest index attaining m (kNone before any non -inf element)
+    int flags;
+};
+
+template <int MODE>
+__device__ __forceinline__ void raise_max(Acc &a, float v, float k) {
+    if (MODE == ROW_SAMPLE) {
+        if (a.m == -INFINITY) {
+            a.s0 = 0.f;
+            a.s1 = 0.f;
+        } else {
+            const float f = ex2((a.m - v) * k);
+            a.s0 *= f;
+            a.s1 *= f;
+        }
+    }
+    a.m = v;
+    a.negm = -v;
+}
+
+// One scalar element (head / tail of a misaligned row).
+template <int MODE>
+__device__ __forceinline__ void proc_scalar(Acc &a, float x, int idx, float k) {
+    if (MODE == ROW_PROBS) {
+        if (!(x >= 0.f && x < INFINITY)) a.flags |= F_NAN;
+        return;
+    }
+    if (x != x) {
+        a.flags |= F_NAN;
+    } else if (x > a.m) {
+        raise_max<MODE>(a, x, k);
+        a.arg = idx;
+    }
+    if (MODE == ROW_SAMPLE) a.s0 += ex2((x + a.negm) * k);
+}
+
+// Eight bf16 values (one 16-byte vector) starting at element e0.
+template <int MODE>
+__device__ __forceinline__ void proc_bf16(Acc &a, const uint4 w, int e0, float k) {
+    const uint32_t mm = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
+    const float vmax = fmax_nan(bf_lo(mm), bf_hi(mm));
+    if (!(vmax <= a.m)) {
+        if (vmax != vmax) {
+            a.flags |= F_NAN;
+        } else {
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            int j = 7;
+#pragma unroll
+            for (int q = 3; q >= 0; --q) {
+                if (bf_hi(ws[q]) == vmax) j = 2 * q + 1;
+                if (bf_lo(ws[q]) == vmax) j = 2 * q;
+            }
+            raise_max<MODE>(a, vmax, k);
+            a.arg = e0 + j;
+        }
+    }
+    if (MODE == ROW_SAMPLE) {
+        float d0, d1, d2, d3, d4, d5, d6, d7;
+        bf_add2(w.x, a.negm, d0, d1);
+        bf_add2(w.y, a.negm, d2, d3);
+        bf_add2(w.z, a.negm, d4, d5);
+        bf_add2(w.w, a.negm, d6, d7);
+        a.s0 += ex2(d0 * k) + ex2(d2 * k) + (ex2(d4 * k) + ex2(d6 * k));
+        a.s1 += ex2(d1 * k) + ex2(d3 * k) + (ex2(d5 * k) + ex2(d7 * k));
+    }
+}
+
+// Four f32 values (one 16-byte vector) starting at element e0.
+template <int MODE>
+__device__ __forceinline__ void proc_f32(Acc &a, const uint4 w, int e0, float k) {
+    const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                        __uint_as_float(w.w)};
+    if (MODE == ROW_PROBS) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (!(x[q] >= 0.f && x[q] < INFINITY)) a.flags |= F_NAN;
+        return;
+    }
+    const float vmax = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
+    if (!(vmax <= a.m)) {
+        if (vmax != vmax) {
+            a.flags |= F_NAN;
+        } else {
+            int j = 3;
+#pragma unroll
+            for (int q = 2; q >= 0; --q)
+                if (x[q] == vmax) j = q;
+            raise_max<MODE>(a, vmax, k);
+            a.arg = e0 + j;
+        }
+    }
+    if (MODE == ROW_SAMPLE) {
+        a.s0 += ex2((x[0] + a.negm) * k) + ex2((x[2] + a.negm) * k);
+        a.s1 += ex2((x[1] + a.negm) * k) + ex2((x[3] + a.negm) * k);
+    }
+}
+
+struct Part {
+    float m, s;
+    int arg, flags;
+};
+
+template <int MODE>
+__device__ __forceinline__ Part merge(Part x, Part y, float k) {
+    Part r;
+    r.m = fmaxf(x.m, y.m);
+    r.flags = x.flags | y.flags;
+    r.arg = x.m > y.m ? x.arg : (y.m > x.m ? y.arg : min(x.arg, y.arg));
+    r.s = 0.f;
+    if (MODE == ROW_SAMPLE && r.m != -INFINITY)
+        r.s = x.s * ex2((x.m - r.m) * k) + y.s * ex2((y.m - r.m) * k);
+    return r;
+}
+
+template <int MODE>
+__device__ __forceinline__ Part warp_merge(Part p, float k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Part q;
+        q.m = shfl_xor(p.m, o);
+        q.s = shfl_xor(p.s, o);
+        q.arg = shfl_xor(p.arg, o);
+        q.flags = shfl_xor(p.flags, o);
+        p = merge<MODE>(p, q, k);
+    }
+    return p;
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kThreads, 3) row_stats_kernel(RowStatsParams P) {
+    constexpr int kEsz = DT == 1 ? 2 : 4;
+    constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t V = P.V;
+    const char *rowp = reinterpret_cast<const char *>(P.x) + (size_t)row * (size_t)V * kEsz;
+
+    __shared__ Part sh_part[kWarps];
+    __shared__ int sh_leaf;
+
+    // Children of this row's node (warp 0): lane handles nodes lane and lane + 32.
+    const bool gather = P.pc != nullptr;
+    const int N = P.N;
+    const int b = row / N, n = row - b * N;
+    int child[2] = {-1, -1};
+    float zc[2] = {0.f, 0.f};
+    if (warp == 0 && (gather || P.skip_leaves)) {
+        bool any = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = lane + 32 * h;
+            if (c >= 1 && c < N && P.parent[(size_t)b * N + c] == n) {
+                any = true;
+                const int t = P.tok[(size_t)b * N + c];
+                if (t >= 0 && t < V) {
+                    child[h] = c;
+                    if (gather) zc[h] = load_elem<DT>(rowp, t);   // prefetch, used at the end
+                }
+            }
+        }
+        if (P.skip_leaves) {
+            const unsigned bal = __ballot_sync(0xffffffffu, any);
+            if (lane == 0) sh_leaf = bal == 0;
+        }
+    }
+    if (P.skip_leaves) {
+        __syncthreads();
+        if (sh_leaf) return;
+    }
+
+    const float k = P.k;
+    Acc a;
+    a.m = -INFINITY;
+    a.negm = 0.f;
+    a.s0 = a.s1 = 0.f;
+    a.arg = kNone;
+    a.flags = 0;
+
+    // Split the row into a scalar head up to 16-byte alignment, vectors, and a scalar tail.
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+    int64_t head = (int64_t)((16 - (addr & 15)) & 15) / kEsz;
+    if (head > V) head = V;
+    const int64_t nvec = (V - head) / kEpv;
+    const int64_t tail0 = head + nvec * kEpv;
+    if (tid < head) proc_scalar<MODE>(a, load_elem<DT>(rowp, tid), tid, k);
+
+    const uint4 *vb = reinterpret_cast<const uint4 *>(rowp + head * kEsz);
+    const int nv = (int)nvec;
+    int i = tid;
+    for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
+        uint4 w[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int e0 = (int)head + (i + u * kThreads) * kEpv;
+            if (DT == 1)
+                proc_bf16<MODE>(a, w[u], e0, k);
+            else
+                proc_f32<MODE>(a, w[u], e0, k);
+        }
+    }
+    for (; i < nv; i += kThreads) {
+        const uint4 w = ldg_stream(vb + i);
+        const int e0 = (int)head + i * kEpv;
+        if (DT == 1)
+            proc_bf16<MODE>(a, w, e0, k);
+        else
+            proc_f32<MODE>(a, w, e0, k);
+    }
+    if (tail0 + tid < V) {
+        const int idx = (int)(tail0 + tid);
+        proc_scalar<MODE>(a, load_elem<DT>(rowp, idx), idx, k);
+    }
+
+    // CTA reduction: warps, then warp 0 over the warp results (fixed order: deterministic).
+    Part p{a.m, a.s0 + a.s1, a.arg, a.flags};
+    p = warp_merge<MODE>(p, k);
+    if (lane == 0) sh_part[warp] = p;
+    __syncthreads();
+    if (warp != 0) return;
+    p = lane < kWarps ? sh_part[lane] : Part{-INFINITY, 0.f, kNone, 0};
+    p = warp_merge<MODE>(p, k);
+
+    if (MODE != ROW_PROBS) {
+        if (p.m == INFINITY) p.flags |= F_POSINF;
+        if (p.m == -INFINITY) p.flags |= F_ALLNEG;
+    }
+    if (lane == 0) {
+        if (P.m) P.m[row] = p.m;
+        if (P.s) P.s[row] = p.s;
+        if (P.arg) P.arg[row] = p.arg == kNone ? 0 : p.arg;
+        P.flags[row] = p.flags;
+    }
+    if (gather) {
+        const float negm = p.m == -INFINITY ? 0.f : -p.m;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (child[h] < 0) continue;
+            float v;
+            if (MODE == ROW_PROBS)
+                v = zc[h];
+            else
+                v = P.pc_normalized ? ex2((zc[h] + negm) * k) / p.s : ex2((zc[h] + negm) * k);
+            P.pc[(size_t)b * N + child[h]] = v;
+        }
+    }
+}
+
+template <int DT, int MODE>
+cudaError_t launch(const RowStatsParams &p, cudaStream_t st) {
+    row_stats_kernel<DT, MODE><<<p.rows, kThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st) {
+    if (p.rows <= 0) return cudaSuccess;
+    if (dtype == 1) {
+        if (mode == ROW_GREEDY) return launch<1, ROW_GREEDY>(p, st);
+        if (mode == ROW_SAMPLE) return launch<1, ROW_SAMPLE>(p, st);
+        return cudaErrorInvalidValue;
+    }
+    if (mode == ROW_GREEDY) return launch<0, ROW_GREEDY>(p, st);
+    if (mode == ROW_SAMPLE) return launch<0, ROW_SAMPLE>(p, st);
+    return launch<0, ROW_PROBS>(p, st);
+}
+
+}  // namespace specv

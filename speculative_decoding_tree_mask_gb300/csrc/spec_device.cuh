@@ -1,0 +1,92 @@
+// Device-side helpers of the verification kernels (sm_103a). Internal to the CUDA path.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spec_internal.h"
+
+namespace specv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kNone = 0x7fffffff;   // "no index yet" in argmax reductions
+
+// 2^x on the special-function unit (flushes denormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Lane-wise max of two bf16 pairs; a NaN in either operand propagates.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// bf16 halves of a packed word widened to float (exact).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// (x + c) for both bf16 halves of w, widened and added in one rounding each.
+__device__ __forceinline__ void bf_add2(uint32_t w, float c, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %3;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(w), "f"(c));
+}
+
+// 16-byte streaming load: read-only path, not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Scalar element load as float (bf16 or f32 storage).
+template <int DT>
+__device__ __forceinline__ float load_elem(const void *row, int64_t i);
+template <>
+__device__ __forceinline__ float load_elem<0>(const void *row, int64_t i) {
+    return __ldg(reinterpret_cast<const float *>(row) + i);
+}
+template <>
+__device__ __forceinline__ float load_elem<1>(const void *row, int64_t i) {
+    uint16_t h = __ldg(reinterpret_cast<const unsigned short *>(row) + i);
+    return __uint_as_float(uint32_t(h) << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ T shfl_xor(T v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+
+// Inclusive warp scan (fixed association: Hillis-Steele over the 32 lanes).
+__device__ __forceinline__ float warp_incl_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+__device__ __forceinline__ double warp_incl_scan_d(double x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+}  // namespace specv

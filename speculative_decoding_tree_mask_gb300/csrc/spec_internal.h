@@ -1,0 +1,78 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels. Internal.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace specv {
+
+constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)
+
+enum RowMode { ROW_GREEDY = 0, ROW_SAMPLE = 1, ROW_PROBS = 2 };
+enum DraftKind { DRAFT_POINT = 0, DRAFT_PROBS_F32 = 1, DRAFT_LOGITS = 2 };
+
+// Row statistics over `rows` rows of V elements (see spec_row_stats in spec_verify.h).
+struct RowStatsParams {
+    const void *x;
+    int64_t V;
+    int rows;
+    int N;                   // nodes per request; rows are (b, n) = (row / N, row % N)
+    float k;                 // log2(e) / T (sampling); unused for greedy / probabilities
+    const int32_t *parent;   // with tok: gather of child probabilities; may be null
+    const int32_t *tok;
+    int skip_leaves;         // rows of nodes without children are not read (draft rows)
+    float *m;
+    float *s;
+    int32_t *arg;
+    int32_t *flags;
+    float *pc;               // child_prob output (indexed by child row); may be null
+    int pc_normalized;       // 1: pc = e_t / S (probability); 0: pc = e_t (walk input)
+};
+
+cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);
+
+cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
+                             int32_t *status, cudaStream_t st);
+
+struct WalkOutputs {
+    int32_t *accept_len;
+    int32_t *out_tokens;
+    int32_t *kv_commit;
+    int32_t *bonus;
+    int32_t *status;
+};
+
+struct GreedyWalkParams {
+    int B, N;
+    int64_t V;
+    const int32_t *parent, *tok;
+    const int32_t *arg, *flags;   // row statistics [B, N]
+    WalkOutputs out;
+};
+
+cudaError_t launch_walk_greedy(const GreedyWalkParams &p, cudaStream_t st);
+
+struct SampleWalkParams {
+    int B, N;
+    int64_t V;
+    int dtype;                    // target logits element type
+    const void *logits;
+    const int32_t *parent, *tok;
+    const float *uniforms;        // [B, N+1]
+    float k;                      // log2(e) / T
+    // target row statistics [B, N] and child probabilities p_parent(tok[c]) [B, N]
+    const float *m, *s, *pc;
+    const int32_t *flags;
+    // dense draft (kind != DRAFT_POINT)
+    int draft_kind, draft_dtype;
+    const void *draft;
+    const float *mq, *sq, *qc;
+    const int32_t *dflags;
+    WalkOutputs out;
+};
+
+// Dynamic shared memory the sampling walk needs for vocabulary size V.
+size_t walk_sample_smem(int64_t V);
+cudaError_t launch_walk_sample(const SampleWalkParams &p, cudaStream_t st);
+
+}  // namespace specv

@@ -113,6 +113,8 @@ def chain(N: int) -> np.ndarray:
 
 
 def _affine_perm(rng: np.random.Generator, V: int):
+    if V == 1:
+        return lambda rank: 0
     while True:
         a = int(rng.integers(1, V))
         if math.gcd(a, V) == 1:
@@ -122,8 +124,9 @@ def _affine_perm(rng: np.random.Generator, V: int):
 
 
 def child_tokens(rng: np.random.Generator, parent: np.ndarray, V: int) -> np.ndarray:
-    """Distinct sibling tokens drawn as Zipf(1.1) ranks through a per-node bijection.
-    The root's token is a placeholder (0)."""
+    """Sibling tokens drawn as Zipf(1.1) ranks through a per-node bijection, distinct among
+    siblings while the vocabulary allows (a node with more children than V tokens repeats
+    tokens). The root's token is a placeholder (0)."""
     N = len(parent)
     tok = np.zeros(N, np.int32)
     for node in range(N):
@@ -133,14 +136,17 @@ def child_tokens(rng: np.random.Generator, parent: np.ndarray, V: int) -> np.nda
         perm = _affine_perm(rng, V)
         used = set()
         for c in kids:
-            while True:
-                rank = int(rng.zipf(1.1)) - 1
-                if rank >= V:
-                    continue
+            if len(used) >= V:
+                t = int(rng.integers(0, V))
+            else:
+                for _ in range(64):
+                    rank = int(rng.zipf(1.1)) - 1
+                    if rank < V and perm(rank) not in used:
+                        break
+                else:   # rare: fall back to the lowest unused rank
+                    rank = next(r for r in range(V) if perm(r) not in used)
                 t = perm(rank)
-                if t not in used:
-                    used.add(t)
-                    break
+                used.add(t)
             tok[c] = t
     return tok
 

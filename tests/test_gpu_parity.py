@@ -1,0 +1,399 @@
+"""CUDA path against the oracle, through the C ABI (needs a GB300 and the built library).
+
+Greedy results, masks and argmax are compared bit for bit; sampling results are identical
+except requests whose oracle decision or inverse-CDF margin is below 1e-6 (counted).
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import golden_io
+import parity as PY
+from oracle import enumerate as E
+from oracle import oracle as O
+from speculative_decoding_tree_mask_gb300 import binding as G
+from speculative_decoding_tree_mask_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def h():
+    G.load()
+    with G.Handle(256, 64, 1 << 21, 0) as handle:
+        yield handle
+
+
+def _to(x, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(DEV).contiguous()
+
+
+# ---- tree mask ---------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [1, 2, 5, 32, 33, 64])
+def test_tree_mask_bit_exact(h, orc, N):
+    rng = np.random.default_rng(N)
+    B = 37
+    parents = [W.random_trie(rng, N, 10, 6) for _ in range(B - 3)]
+    parents.append(W.chain(N))
+    parents.append(np.array([-1] + [0] * (N - 1), np.int32))   # star
+    bad = W.random_trie(rng, N, 10, 6)
+    if N > 1:
+        bad[N - 1] = N - 1                                         # parent not before child
+    else:
+        bad[0] = 0
+    parents.append(bad)
+    parent = np.stack(parents).astype(np.int32)
+    out = G.build_tree_mask(h, _to(parent))
+    torch.cuda.synchronize()
+    anc, depth, status = orc.build_mask(parent)
+    assert np.array_equal(out["anc_mask"].cpu().numpy().view(np.uint64), anc)
+    assert np.array_equal(out["depth"].cpu().numpy(), depth)
+    assert np.array_equal(out["status"].cpu().numpy(), status)
+    assert status[-1] == 1 and (status[:-1] == 0).all()
+
+
+# ---- hand-worked goldens through the GPU --------------------------------------------------------
+
+@pytest.mark.parametrize("name", golden_io.names())
+def test_golden_on_gpu(h, name):
+    g = golden_io.load(name)
+    if g["op"] == "mask":
+        out = G.build_tree_mask(h, _to(g["parent"]))
+        torch.cuda.synchronize()
+        got = dict(anc=out["anc_mask"].cpu().numpy().view(np.uint64),
+                   depth=out["depth"].cpu().numpy(), status=out["status"].cpu().numpy())
+    elif g["op"] == "greedy":
+        got = PY.gpu_greedy(h, _to(g["logits"]), _to(g["draft_token"]), _to(g["parent"]))
+    else:
+        kind = {"probs_f32": G.SPEC_DRAFT_PROBS_F32, "logits": G.SPEC_DRAFT_LOGITS}.get(
+            g.get("draft_kind"), G.SPEC_DRAFT_POINT)
+        draft = _to(g["draft"]) if "draft" in g else None
+        got = PY.gpu_sample(h, _to(g["logits"]), _to(g["draft_token"]), _to(g["parent"]),
+                            g["temperature"], _to(g["uniforms"]), draft, kind)
+    assert golden_io.mismatches(g, got) == []
+
+
+# ---- greedy -------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_chain", "greedy_trie"])
+def test_greedy_workloads_bit_exact(h, orc, name):
+    w = W.WORKLOADS[name]
+    x = W.make(w, device=DEV)
+    gpu = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
+    ref = orc.verify_greedy(PY.host(x["logits"]), x["tok_np"], x["parent_np"])
+    PY.assert_exact(gpu, ref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [1, 3, 8, 9, 255, 256, 257, 1000, 4097, 151936])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_greedy_ragged_vocab_and_misaligned_rows(h, orc, dtype, V, offset):
+    w = W.WORKLOADS["greedy_trie"].scaled(B=5, N=9, V=V, dtype=dtype, boost=15.0, seed=V + offset)
+    x = W.make(w, device=DEV)
+    flat = torch.empty(w.B * w.N * V + offset, dtype=w.torch_dtype, device=DEV)
+    logits = flat[offset:].view(w.B, w.N, V)
+    logits.copy_(x["logits"])
+    gpu = PY.gpu_greedy(h, logits, x["draft_token"], x["parent"])
+    ref = orc.verify_greedy(PY.host(x["logits"]), x["tok_np"], x["parent_np"])
+    PY.assert_exact(gpu, ref)
+
+
+def test_greedy_planted_ties_lowest_index(h, orc):
+    B, N, V = 8, 4, 152064
+    rng = np.random.default_rng(3)
+    logits = torch.randn((B, N, V), device=DEV).to(torch.bfloat16)
+    parent = np.tile(W.chain(N), (B, 1))
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for i in range(N):
+            pos = np.sort(rng.choice(V, size=4, replace=False))
+            logits[b, i, torch.as_tensor(pos, device=DEV)] = 9.0
+            if i + 1 < N:
+                tok[b, i + 1] = pos[0]
+    gpu = PY.gpu_greedy(h, logits, _to(tok), _to(parent))
+    ref = orc.verify_greedy(PY.host(logits), tok, parent)
+    PY.assert_exact(gpu, ref)
+    assert (gpu["accept_len"] == N - 1).all()
+
+
+def test_off_path_rows_may_hold_nan(h, orc):
+    w = W.WORKLOADS["greedy_trie"].scaled(B=16, V=5000, boost=30.0, seed=77)
+    x = W.make(w, device=DEV)
+    ref = orc.verify_greedy(PY.host(x["logits"]), x["tok_np"], x["parent_np"])
+    logits = x["logits"].clone()
+    for b in range(w.B):
+        on_path = set(ref["kv_commit"][b][ref["kv_commit"][b] >= 0].tolist())
+        for i in range(w.N):
+            if i not in on_path:
+                logits[b, i] = float("nan")
+    gpu = PY.gpu_greedy(h, logits, x["draft_token"], x["parent"])
+    PY.assert_exact(gpu, ref)
+    assert (gpu["status"] == 0).all()
+
+
+# ---- row statistics -----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 2.0])
+@pytest.mark.parametrize("dtype,V", [("bf16", 151936), ("f32", 4099), ("bf16", 77)])
+def test_row_stats_against_oracle(h, orc, T, dtype, V):
+    w = W.WORKLOADS["sampling_trie"].scaled(B=6, N=16, V=V, dtype=dtype, seed=V)
+    x = W.make(w, device=DEV)
+    logits = x["logits"]
+    logits[0, 3] = float("-inf")                       # all -inf row
+    logits[1, 2, V // 2] = float("nan")                # NaN row
+    logits[2, 5, V - 1] = float("inf")                 # +inf row
+    logits[3, 1, : V // 2] = float("-inf")             # partly -inf
+    rows = w.B * w.N
+    m = torch.empty(rows, device=DEV)
+    s = torch.empty(rows, device=DEV)
+    a = torch.empty(rows, dtype=torch.int32, device=DEV)
+    f = torch.empty(rows, dtype=torch.int32, device=DEV)
+    pc = torch.full((w.B, w.N), -1.0, device=DEV)
+    G.spec_row_stats(h, logits, w.N, T, m, s, a, f, x["draft_token"], x["parent"], pc)
+    torch.cuda.synchronize()
+    hl = PY.host(logits).reshape(rows, V)
+    m, s, a, f, pc = (t.cpu().numpy() for t in (m, s, a, f, pc))
+    for r in range(rows):
+        om, oS, oa, obad = orc.row_stats(hl[r], T)
+        assert (f[r] != 0) == bool(obad), r
+        if obad:
+            continue
+        assert m[r] == om and a[r] == oa, r
+        assert abs(s[r] - oS) <= 1e-5 * oS, (r, s[r], oS)
+    for b in range(w.B):
+        for c in range(1, w.N):
+            par = x["parent_np"][b, c]
+            r = b * w.N + par
+            if orc.row_stats(hl[r], T)[3]:
+                continue
+            p = orc.row_softmax(hl[r], T)[x["tok_np"][b, c]]
+            assert abs(pc[b, c] - p) <= 1e-5 * p + 1e-30, (b, c, pc[b, c], p)
+
+
+# ---- sampling, point-mass drafts ----------------------------------------------------------------
+
+@pytest.mark.parametrize("T,boost", [(0.7, 8.0), (0.7, 30.0), (1.0, 12.0), (1.8, 20.0)])
+def test_sample_point_trie(h, orc, T, boost):
+    w = W.WORKLOADS["sampling_trie"].scaled(temperature=T, boost=boost, seed=int(T * 100 + boost))
+    x = W.make(w, device=DEV)
+    gpu = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"])
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"])
+    PY.compare_sample(gpu, ref)
+
+
+def test_sample_point_many_small_requests(h, orc):
+    w = W.WORKLOADS["sampling_trie"].scaled(B=256, N=24, V=3001, dtype="f32", boost=6.0,
+                                            sigma=1.5, temperature=1.0, seed=9)
+    x = W.make(w, device=DEV)
+    gpu = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"])
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"])
+    PY.compare_sample(gpu, ref)
+    assert gpu["accept_len"].max() >= 2
+
+
+def test_sample_rejected_mass_resummed(h, orc):
+    """The first child holds almost all the mass and is rejected: the next sibling's
+    denominator is re-summed over the row."""
+    B, N, V = 8, 4, 151936
+    logits = (3.0 * torch.randn((B, N, V), device=DEV)).to(torch.bfloat16)
+    parent = np.tile(np.array([-1, 0, 0, 0], np.int32), (B, 1))
+    tok = np.tile(np.array([0, 11, 22, 33], np.int32), (B, 1))
+    logits[:, 0, 11] = 20.0
+    logits[:, 0, 22] = 3.0
+    u = torch.rand((B, N + 1), device=DEV)
+    u[:, 1] = 0.99999
+    gpu = PY.gpu_sample(h, logits, _to(tok), _to(parent), 1.0, u)
+    ref = PY.oracle_sample(orc, logits, _to(tok), _to(parent), 1.0, u)
+    PY.compare_sample(gpu, ref)
+
+
+def test_temperature_zero_is_greedy(h):
+    w = W.WORKLOADS["sampling_trie"].scaled(boost=25.0, seed=4)
+    x = W.make(w, device=DEV)
+    a = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
+    b = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 0.0, x["uniforms"])
+    for k in PY.KEYS:
+        assert np.array_equal(a[k], b[k])
+
+
+def test_sampling_is_deterministic(h):
+    w = W.WORKLOADS["sampling_trie"].scaled(boost=12.0, seed=5)
+    x = W.make(w, device=DEV)
+    a = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 0.7, x["uniforms"])
+    b = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 0.7, x["uniforms"])
+    for k in PY.KEYS:
+        assert np.array_equal(a[k], b[k])
+
+
+# ---- sampling, dense drafts --------------------------------------------------------------------
+
+def test_dense_chain_logits(h, orc):
+    w = W.WORKLOADS["dense_chain"]
+    x = W.make(w, device=DEV)
+    gpu = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"],
+                        x["draft"], G.SPEC_DRAFT_LOGITS)
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"],
+                           x["draft"], G.SPEC_DRAFT_LOGITS)
+    PY.compare_sample(gpu, ref)
+
+
+@pytest.mark.parametrize("V", [1000, 4103])
+def test_dense_chain_probs(h, orc, V):
+    w = W.WORKLOADS["dense_chain"].scaled(B=32, V=V, dtype="f32", seed=V)
+    x = W.make(w, device=DEV)
+    probs = torch.softmax(x["draft"].float().cpu(), dim=-1).contiguous()
+    probs[:, -1] = float("nan")            # the leaf's draft row is never read
+    gpu = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"],
+                        probs.to(DEV), G.SPEC_DRAFT_PROBS_F32)
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"],
+                           probs, G.SPEC_DRAFT_PROBS_F32)
+    PY.compare_sample(gpu, ref)
+    assert (gpu["status"] == 0).all()
+
+
+def test_dense_tree_logits(h, orc):
+    """Dense drafts on trees: siblings tested against successive residual levels."""
+    rng = np.random.default_rng(8)
+    B, N, V, T = 64, 12, 3000, 1.0
+    parent = np.stack([W.random_trie(rng, N, 3, 4) for _ in range(B)])
+    target = torch.randn((B, N, V), generator=torch.Generator().manual_seed(1)) * 1.0
+    draft = target + 0.7 * torch.randn((B, N, V), generator=torch.Generator().manual_seed(2))
+    probs = torch.softmax(draft / T, dim=-1)
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            tok[b, c] = int(torch.multinomial(probs[b, parent[b, c]], 1,
+                                              generator=torch.Generator().manual_seed(b * N + c)))
+    u = torch.rand((B, N + 1), generator=torch.Generator().manual_seed(3))
+    args = (_to(target), _to(tok), _to(parent), T, _to(u))
+    gpu = PY.gpu_sample(h, *args, _to(draft), G.SPEC_DRAFT_LOGITS)
+    ref = PY.oracle_sample(orc, *args, draft, G.SPEC_DRAFT_LOGITS)
+    PY.compare_sample(gpu, ref)
+
+
+# ---- full-size large-tree workload ----------------------------------------------------------------
+
+def test_large_tree_full_size(h, orc):
+    w = W.WORKLOADS["large_tree"]
+    x = W.make(w, device=DEV)
+    T = w.temperature
+    gpu = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"])
+    # every request: structural properties of the result
+    _, depth, _ = orc.build_mask(x["parent_np"])
+    for b in range(w.B):
+        par, tok = x["parent_np"][b], x["tok_np"][b]
+        L = gpu["accept_len"][b]
+        kv = gpu["kv_commit"][b]
+        assert gpu["status"][b] == 0 and 0 <= L <= depth[b].max()
+        assert kv[0] == 0 and all(par[kv[j + 1]] == kv[j] for j in range(L))
+        assert (gpu["out_tokens"][b, :L] == tok[kv[1:L + 1]]).all()
+        kids = [c for c in range(w.N) if par[c] == kv[L]]
+        assert gpu["bonus"][b] not in tok[kids]       # rejected tokens leave the residual
+    # a sample of requests against the oracle
+    rows = np.r_[0:8, np.random.default_rng(0).choice(np.arange(8, w.B), 8, replace=False)]
+    ridx = torch.as_tensor(rows, device=DEV)
+    ref = PY.oracle_sample(orc, x["logits"][ridx], x["draft_token"][ridx], x["parent"][ridx], T,
+                           x["uniforms"][ridx])
+    PY.compare_sample(gpu, ref, rows=rows)
+    # greedy on the same sample
+    gg = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
+    gref = orc.verify_greedy(PY.host(x["logits"][ridx]), x["tok_np"][rows], x["parent_np"][rows],
+                             nthreads=8)
+    PY.assert_exact(gg, gref, rows=rows)
+
+
+# ---- losslessness on the GPU (Monte Carlo against the exact law) --------------------------------
+
+def _chi2(samples, law):
+    from test_oracle_lossless import _chi2_pvalue
+    return _chi2_pvalue(samples, law)
+
+
+def test_gpu_point_mass_law(orc):
+    parent, tokens = [-1, 0, 0, 0, 1, 2], [0, 2, 0, 3, 1, 1]
+    V, T, n = 5, 0.9, 100_000
+    model = E.SyntheticLM(V, seed=101, scale=1.3)
+    rows = torch.as_tensor(E.tree_rows(model, tokens, parent))
+    logits = rows.expand(n, -1, -1).contiguous().to(DEV)
+    u = torch.rand((n, len(parent) + 1), generator=torch.Generator().manual_seed(5)).to(DEV)
+    with G.Handle(n, 8, 64) as hh:
+        out = PY.gpu_sample(hh, logits, _to(np.tile(tokens, (n, 1)).astype(np.int32)),
+                            _to(np.tile(parent, (n, 1)).astype(np.int32)), T, u)
+    seqs = [tuple(out["out_tokens"][i, :out["accept_len"][i] + 1]) for i in range(n)]
+    assert _chi2(seqs, E.verify_point_dist(model, tokens, parent, T)) > 1e-5
+
+
+def test_gpu_dense_chain_law(orc):
+    k, V, T, n = 2, 4, 1.0, 100_000
+    model, draft = E.SyntheticLM(V, seed=31, scale=1.5), E.SyntheticLM(V, seed=32, scale=1.5)
+    parent = [-1] + list(range(k))
+    chains = list(itertools.product(range(V), repeat=k))
+    wts = []
+    for xs in chains:
+        pw, pre = 1.0, ()
+        for t in xs:
+            pw *= draft.probs(pre, T)[t]
+            pre += (t,)
+        wts.append(pw)
+    rng = np.random.default_rng(6)
+    pick = rng.choice(len(chains), size=n, p=np.array(wts) / sum(wts))
+    rows = np.stack([E.tree_rows(model, (0,) + xs, parent) for xs in chains])[pick]
+    drows = np.stack([E.tree_rows(draft, (0,) + xs, parent) for xs in chains])[pick]
+    toks = np.array([(0,) + xs for xs in chains], np.int32)[pick]
+    u = rng.random((n, k + 2), dtype=np.float32)
+    with G.Handle(n, 8, 64) as hh:
+        out = PY.gpu_sample(hh, _to(rows), _to(toks), _to(np.tile(parent, (n, 1)).astype(np.int32)),
+                            T, _to(u), _to(drows), G.SPEC_DRAFT_LOGITS)
+    seqs = [tuple(out["out_tokens"][i, :out["accept_len"][i] + 1]) for i in range(n)]
+    assert _chi2(seqs, E.dense_chain_mixture(model, draft, k, T)) > 1e-5
+
+
+# ---- API behaviour ---------------------------------------------------------------------------------
+
+def test_host_argument_errors(h):
+    w = W.WORKLOADS["sampling_trie"].scaled(B=2, N=4, V=100, seed=1)
+    x = W.make(w, device=DEV)
+    out = G.alloc_outputs(2, 4, DEV)
+    with pytest.raises(G.SpecError) as e:
+        G.verify_sample(h, x["logits"], x["draft_token"], x["parent"], -1.0, x["uniforms"])
+    assert e.value.code == G.SPEC_ERR_ARG
+    with pytest.raises(G.SpecError):
+        G.verify_sample(h, x["logits"], x["draft_token"], x["parent"], float("nan"), x["uniforms"])
+    with pytest.raises(G.SpecError):
+        G.verify_sample(h, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"],
+                        draft=None, draft_kind=G.SPEC_DRAFT_LOGITS)
+    big = torch.zeros((257, 4, 100), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(G.SpecError):
+        G.verify_greedy(h, big, torch.zeros((257, 4), dtype=torch.int32, device=DEV),
+                        torch.zeros((257, 4), dtype=torch.int32, device=DEV))
+    with pytest.raises(G.SpecError) as e:
+        G.Handle(4, 65, 100)
+    assert e.value.code == G.SPEC_ERR_UNSUPPORTED
+    # B == 0 is a no-op
+    G.spec_verify_greedy(h, x["logits"][:0], x["draft_token"][:0], x["parent"][:0],
+                         out["accept_len"], out["out_tokens"], out["kv_commit"], out["bonus"],
+                         out["status"])
+
+
+def test_side_stream_and_profiling(h):
+    w = W.WORKLOADS["sampling_trie"].scaled(B=4, N=8, V=20000, seed=2)
+    x = W.make(w, device=DEV)
+    s = torch.cuda.Stream()
+    ref = PY.gpu_sample(h, x["logits"], x["draft_token"], x["parent"], 0.7, x["uniforms"])
+    G.spec_profile_begin(h)
+    with torch.cuda.stream(s):
+        out = G.verify_sample(h, x["logits"], x["draft_token"], x["parent"], 0.7, x["uniforms"],
+                              stream=s)
+    s.synchronize()
+    prof = G.spec_profile_end(h)
+    assert prof["row_stats"][1] == 1 and prof["walk_sample"][1] == 1
+    assert prof["row_stats"][0] > 0
+    for k in PY.KEYS:
+        assert np.array_equal(out[k].cpu().numpy(), ref[k])
