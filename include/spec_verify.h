@@ -173,6 +173,28 @@ int spec_profile_end(spec_handle h, float *ms_per_class, int32_t *launches_per_c
 /* Static description of a SPEC_ERR_* code. */
 const char *spec_error_string(int code);
 
+/*
+ * Greedy verification that allocates nothing. The pages have no counterpart of this entry
+ * point; it exists for callers that cannot call cudaMalloc, for example plugins inside an
+ * engine that reserves all device memory up front and hands a kernel only its tensors, or
+ * latency-critical loops that cannot accept cudaMalloc's implicit device synchronisation.
+ *
+ * Same arguments, results and status codes as spec_verify_greedy, but no handle: it runs on
+ * the current device, and the per-row scratch (argmax and flags of each of the B*N rows) is
+ * a static device array of SPEC_NOALLOC_MAX_ROWS rows (128 KiB) that every GPU loading the
+ * library holds until the process exits. B*N > SPEC_NOALLOC_MAX_ROWS returns SPEC_ERR_ARG
+ * and launches nothing. No cudaMalloc, cudaFree or allocating library call is made.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * once; make that first call before any stream capture. All calls share the one array
+ * (each call writes every row it reads, so stale contents do not matter), so calls that
+ * overlap on the GPU, on any streams, race: serialise them.
+ */
+#define SPEC_NOALLOC_MAX_ROWS 16384
+int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, int N, int64_t V,
+                               const int32_t *draft_token, const int32_t *parent,
+                               int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
+                               int32_t *bonus, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

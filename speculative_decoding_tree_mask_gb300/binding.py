@@ -233,3 +233,26 @@ def build_tree_mask(h: Handle, parent, stream=None) -> dict:
                status=torch.empty(B, dtype=torch.int32, device=dev))
     spec_build_tree_mask(h, parent, out["anc_mask"], out["depth"], out["status"], stream)
     return out
+
+
+# ---- greedy verification without device allocation --------------------------------------------
+
+SPEC_NOALLOC_MAX_ROWS = 16384
+
+
+def spec_verify_greedy_noalloc(logits, draft_token, parent, accept_len, out_tokens, kv_commit,
+                               bonus, status, stream=None):
+    """Greedy verification whose scratch is a static device array (no cudaMalloc anywhere),
+    for callers that must not allocate device memory. Runs on the tensors' device, which must
+    be the current device; B*N <= SPEC_NOALLOC_MAX_ROWS. Calls share the scratch, so calls
+    that overlap on the GPU race."""
+    lib = load()
+    fn = lib.spec_verify_greedy_noalloc
+    if fn.argtypes is None:
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        fn.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+    B, N, V = logits.shape
+    _check(fn(_ptr(logits), _dtype_code(logits), B, N, V, _ptr(_i32(draft_token, "draft_token")),
+              _ptr(_i32(parent, "parent")), _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit),
+              _ptr(bonus), _ptr(status), _stream(stream, logits.device)),
+           "spec_verify_greedy_noalloc")
