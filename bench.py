@@ -211,6 +211,8 @@ def bench_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
     w = W.WORKLOADS[WORKLOAD]
+    if args.requests:
+        w = w.scaled(B=args.requests)
     x = W.make(w, device=dev, seed=w.seed + rank)
     B, N, V, T = w.B, w.N, w.V, w.temperature
     h = G.Handle(B, N, V, local)
@@ -334,6 +336,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="requests per rank (default: the workload's 256); for profiling runs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

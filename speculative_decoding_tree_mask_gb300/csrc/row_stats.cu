@@ -11,7 +11,8 @@
 // does not exceed the running max costs 4 packed max instructions; otherwise (rare: O(log n)
 // times per thread) the sum is rescaled. Elements are visited in increasing index order per
 // thread, so a strict '>' keeps the lowest index; partial results merge lowest-index-first.
-// The stream is HBM-bound: 16-byte read-only loads, 4 in flight per thread, 512 threads.
+// The stream is HBM-bound: 16-byte read-only loads, 4 in flight per thread, 256 threads per
+// CTA and 6 CTAs per SM (24 KiB of loads in flight per CTA).
 
 #include <cfloat>
 
@@ -21,7 +22,7 @@
 namespace specv {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
 
@@ -160,7 +161,7 @@ __device__ __forceinline__ Part warp_merge(Part p, float k) {
 }
 
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kThreads, 3) row_stats_kernel(RowStatsParams P) {
+__global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
     const int row = blockIdx.x;

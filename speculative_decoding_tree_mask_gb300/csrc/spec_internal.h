@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "spec_verify.h"
+
 namespace specv {
 
 constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)

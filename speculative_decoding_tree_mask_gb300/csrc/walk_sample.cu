@@ -1,0 +1,685 @@
+// Sampling tree walk, inverse-CDF bonus draw and accepted-path compaction.
+//
+// EmbodiInfer PR #11 "perf(activevln): grammar-trie speculation and lossless throughput",
+// commit 4b728e2: sampling uses standard (SpecInfer-style) rejection sampling against the
+// draft, so the output distribution is the target's. From the root the walk tests the
+// children of the current node in ascending node index; an accepted child becomes the
+// current node; when no child is accepted (or the node is a leaf) a bonus token is drawn
+// from the residual distribution by inverse CDF with the request's last uniform.
+//
+// One CTA of 512 threads per request. Warp 0 runs the walk on scalars gathered by the
+// row-statistics kernel (e_t = 2^((z_t - m) log2(e)/T) at every child token, the row sums S,
+// and the same for dense draft rows); the children of a node are one 64-bit ballot mask.
+// Whenever a decision needs a sum over the vocabulary, all 16 warps stream the node's row
+// once ("pass"):
+//   * point drafts: p(t) / sum_{v not in R} p(v) is formed as e_t / (S - sum_{v in R} e_v);
+//     when the rejected mass exceeds 15/16 of the denominator the remainder is re-summed;
+//   * dense drafts: after a rejection with siblings left, Z = sum_v max(r(v) - q(v), 0)
+//     normalises the next residual level;
+//   * bonus: the residual at the stop node is summed per 256-element sub-tile (a warp scan
+//     over 32 lanes x 8 elements), the sub-tile sums stay in shared memory, warp 0 locates
+//     the sub-tile holding tau = u * S (scan of per-lane chunk sums, then of the chosen
+//     chunk) and re-reads only that sub-tile to find the token.
+// Every search level falls back to the last token with r(v) > 0 when rounding leaves tau past
+// its end, so the drawn token always has positive residual mass.
+// A pass issues the 16-byte loads of 8 sub-tiles per lane before using any of them (2 CTAs
+// per SM: 128 KiB of each SM's loads in flight); sums use compensated float32, and the
+// float64 pipe (slow on this part) only sees a handful of operations per decision.
+
+#include <climits>
+
+#include "spec_device.cuh"
+#include "spec_internal.h"
+
+namespace specv {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSub = 256;   // elements per sub-tile: 32 lanes x 8
+
+enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z };
+
+struct Smem {
+    int par[kMaxN], tok[kMaxN], flags[kMaxN], dflags[kMaxN];
+    float ec[kMaxN];     // e_t of each child in its parent's target row
+    float eqc[kMaxN];    // draft: e_q at each child token (probabilities: q itself)
+    float s[kMaxN], m[kMaxN], sq[kMaxN], mq[kMaxN];
+    float u[kMaxN + 1];
+    int path[kMaxN];
+    int R[kMaxN];        // rejected tokens at the current node, ascending
+    float invZ[kMaxN];   // dense: 1 / Z of each normalised residual level (0: level kept)
+    double zinv[kMaxN];  // dense: 1 / Z of each level in float64 (0: level kept)
+    int nR, nlev, pending;
+    int cmd, node, L, st, bonus;
+    double total;
+    double wtot[kWarps];
+};
+
+struct Ctx {
+    const char *zrow;    // target row of the node
+    const char *drow;    // draft row of the node (dense drafts)
+    float negm, invS, negmq, invSq, k;
+    int V;
+    bool zvec, dvec;     // rows 16-byte aligned
+    bool useq;           // dense residual levels present: the draft row is read
+};
+
+// ---- element access -------------------------------------------------------------------------
+
+template <int DT>
+__device__ __forceinline__ void fetch(const char *row, int e0, uint4 &a, uint4 &b) {
+    if (DT == 1) {
+        a = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 8);
+    } else {
+        a = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4);
+        b = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4 + 1);
+    }
+}
+
+// x[q] = value(e0 + q) + c for 8 elements held in one (bf16) or two (f32) 16-byte vectors.
+template <int DT>
+__device__ __forceinline__ void shifted8(const uint4 &a, const uint4 &b, float c, float (&x)[8]) {
+    if (DT == 1) {
+        bf_add2(a.x, c, x[0], x[1]);
+        bf_add2(a.y, c, x[2], x[3]);
+        bf_add2(a.z, c, x[4], x[5]);
+        bf_add2(a.w, c, x[6], x[7]);
+    } else {
+        x[0] = __uint_as_float(a.x) + c; x[1] = __uint_as_float(a.y) + c;
+        x[2] = __uint_as_float(a.z) + c; x[3] = __uint_as_float(a.w) + c;
+        x[4] = __uint_as_float(b.x) + c; x[5] = __uint_as_float(b.y) + c;
+        x[6] = __uint_as_float(b.z) + c; x[7] = __uint_as_float(b.w) + c;
+    }
+}
+
+// The same with scalar loads; positions at or beyond V read as `fill` (before the shift).
+template <int DT>
+__device__ __forceinline__ void shifted8_scalar(const char *row, int e0, int V, float c,
+                                                float fill, float (&x)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = (e0 + q < V ? load_elem<DT>(row, e0 + q) : fill) + c;
+}
+
+// Residual r(v) of 8 elements from the shifted target values zs = z - m and, for dense drafts,
+// the shifted draft values ds = d - m_q (logits) or the draft probabilities (PROBS_F32).
+template <int DK>
+__device__ __forceinline__ void residual8(const Ctx &c, const Smem &sm, const float (&zs)[8],
+                                          const float (&ds)[8], float (&r)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float e = ex2(zs[q] * c.k);
+        if (DK == DRAFT_POINT) {
+            r[q] = e;
+        } else {
+            float x = e * c.invS;
+            if (c.useq) {
+                const float qv = DK == DRAFT_LOGITS ? ex2(ds[q] * c.k) * c.invSq : ds[q];
+                for (int l = 0; l < sm.nlev; ++l)
+                    if (sm.invZ[l] > 0.f) x = fmaxf(x - qv, 0.f) * sm.invZ[l];
+                if (sm.pending) x = fmaxf(x - qv, 0.f);
+            }
+            r[q] = x;
+        }
+    }
+}
+
+// Point drafts: zero the rejected tokens inside sub-tile j. `rc` is a warp-uniform cursor
+// into the ascending rejected list (sub-tiles of one warp are visited in increasing order).
+__device__ __forceinline__ void zero_rejected(const Smem &sm, int j, int lane, int &rc,
+                                              float (&r)[8]) {
+    const int lo = j * kSub, hi = lo + kSub;
+    const int nR = sm.nR;
+    while (rc < nR && sm.R[rc] < lo) ++rc;
+    if (rc < nR && sm.R[rc] < hi) {
+        const int e0 = lo + lane * 8;
+        for (int i = rc; i < nR && sm.R[i] < hi; ++i) {
+            const int t = sm.R[i] - e0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (t == q) r[q] = 0.f;
+        }
+    }
+}
+
+// Residual of the 8 elements of sub-tile j owned by this lane, with every check needed when
+// the sub-tile may be ragged or the rows unaligned.
+template <int DT, int DK, int DDT>
+__device__ __forceinline__ void residual8_any(const Ctx &c, const Smem &sm, int j, int lane,
+                                              int &rc, float (&r)[8]) {
+    constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
+    const int e0 = j * kSub + lane * 8;
+    float zs[8], ds[8];
+    const bool vec = c.zvec && (DK == DRAFT_POINT || !c.useq || c.dvec) && e0 + 8 <= c.V;
+    if (vec) {
+        uint4 za, zb, da, db;
+        fetch<DT>(c.zrow, e0, za, zb);
+        if (DK != DRAFT_POINT && c.useq) fetch<kDDT>(c.drow, e0, da, db);
+        shifted8<DT>(za, zb, c.negm, zs);
+        if (DK == DRAFT_LOGITS && c.useq) shifted8<kDDT>(da, db, c.negmq, ds);
+        if (DK == DRAFT_PROBS_F32 && c.useq) shifted8<0>(da, db, 0.f, ds);
+    } else {
+        shifted8_scalar<DT>(c.zrow, e0, c.V, c.negm, -INFINITY, zs);
+        if (DK == DRAFT_LOGITS && c.useq)
+            shifted8_scalar<kDDT>(c.drow, e0, c.V, c.negmq, -INFINITY, ds);
+        if (DK == DRAFT_PROBS_F32 && c.useq) shifted8_scalar<0>(c.drow, e0, c.V, 0.f, 0.f, ds);
+    }
+    residual8<DK>(c, sm, zs, ds, r);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (e0 + q >= c.V) r[q] = 0.f;
+    if (DK == DRAFT_POINT) zero_rejected(sm, j, lane, rc, r);
+}
+
+// Compensated (Kahan) float accumulation: the error stays near one float rounding however
+// many terms are added, without the slow float64 pipe.
+struct KSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const float y = x - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+    }
+    __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+};
+
+__device__ __forceinline__ float sum8(const float (&r)[8]) {
+    float ls = r[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) ls += r[q];
+    return ls;
+}
+
+// ---- one pass over the node's residual ----------------------------------------------------
+
+// Every warp sums its sub-tiles into subsum[] (one warp scan per 256 elements); the CTA total
+// lands in sm.total. All threads call it; it ends synchronised.
+template <int DT, int DK, int DDT>
+__device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum) {
+    // sub-tiles in flight per warp (32 registers of raw loads)
+    constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : 2;
+    constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nsub = (c.V + kSub - 1) / kSub;
+    const bool vec = c.zvec && (DK == DRAFT_POINT || !c.useq || c.dvec);
+    const int nfull = vec ? c.V / kSub : 0;
+    KSum wsum;
+    int rc = 0;
+
+    for (int j0 = warp; j0 < nfull; j0 += kWarps * U) {
+        uint4 za[U], zb[U], da[U], db[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kWarps;
+            if (j < nfull) {
+                const int e0 = j * kSub + lane * 8;
+                fetch<DT>(c.zrow, e0, za[u], zb[u]);
+                if (DK != DRAFT_POINT && c.useq) fetch<kDDT>(c.drow, e0, da[u], db[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kWarps;
+            if (j < nfull) {
+                float zs[8], ds[8], r[8];
+                shifted8<DT>(za[u], zb[u], c.negm, zs);
+                if (DK == DRAFT_LOGITS && c.useq) shifted8<kDDT>(da[u], db[u], c.negmq, ds);
+                if (DK == DRAFT_PROBS_F32 && c.useq) shifted8<0>(da[u], db[u], 0.f, ds);
+                residual8<DK>(c, sm, zs, ds, r);
+                if (DK == DRAFT_POINT) zero_rejected(sm, j, lane, rc, r);
+                const float incl = warp_incl_scan(sum8(r));
+                if (lane == 31) {
+                    subsum[j] = incl;
+                    wsum.add(incl);
+                }
+            }
+        }
+    }
+    // Ragged last sub-tile, or every sub-tile of a row that is not 16-byte aligned.
+    for (int j = nfull + warp; j < nsub; j += kWarps) {
+        float r[8];
+        residual8_any<DT, DK, DDT>(c, sm, j, lane, rc, r);
+        const float incl = warp_incl_scan(sum8(r));
+        if (lane == 31) {
+            subsum[j] = incl;
+            wsum.add(incl);
+        }
+    }
+
+    if (lane == 31) sm.wtot[warp] = wsum.value();
+    __syncthreads();
+    if (warp == 0) {
+        double t = lane < kWarps ? sm.wtot[lane] : 0.0;
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) sm.total = t;
+    }
+    __syncthreads();
+}
+
+// Largest token with r > 0 (warp 0), from the stored sub-tile sums: the fallback when rounding
+// leaves tau at the very end of the row. -1 if the residual is zero everywhere.
+template <int DT, int DK, int DDT>
+__device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum) {
+    const int lane = threadIdx.x & 31;
+    const int nsub = (c.V + kSub - 1) / kSub;
+    int jl = -1;
+    for (int j = lane; j < nsub; j += 32)
+        if (subsum[j] > 0.f) jl = j;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) jl = max(jl, shfl_xor(jl, o));
+    if (jl < 0) return -1;
+    float r[8];
+    int rc = 0;
+    residual8_any<DT, DK, DDT>(c, sm, jl, lane, rc, r);
+    int lk = -1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (r[q] > 0.f) lk = jl * kSub + lane * 8 + q;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lk = max(lk, shfl_xor(lk, o));
+    return lk;
+}
+
+// Inverse CDF over the stored sub-tile sums (warp 0): the bonus token for uniform u, or -1
+// when the residual sums to zero.
+template <int DT, int DK, int DDT>
+__device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, float u) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int nsub = (c.V + kSub - 1) / kSub;
+    // level 1: every lane sums a contiguous chunk of sub-tiles; scan the chunk totals
+    const int cs = (nsub + 31) / 32;
+    const int lo = min(lane * cs, nsub), hi = min(lo + cs, nsub);
+    KSum chunk;
+    for (int j = lo; j < hi; ++j) chunk.add(subsum[j]);
+    const double incl = warp_incl_scan_d(chunk.value());
+    const double S = __shfl_sync(full, incl, 31);
+    if (!(S > 0.0)) return -1;
+    double excl = __shfl_up_sync(full, incl, 1);
+    if (lane == 0) excl = 0.0;
+    const double tau = (double)u * S;
+    const unsigned ball = __ballot_sync(full, incl > tau);
+    if (ball == 0) return last_positive<DT, DK, DDT>(c, sm, subsum);
+    const int owner = __ffs(ball) - 1;
+    const int olo = __shfl_sync(full, lo, owner), ohi = __shfl_sync(full, hi, owner);
+    double base = __shfl_sync(full, excl, owner);
+    // level 2: the owner's chunk, 32 sub-tiles at a time, one lane per sub-tile
+    int js = -1, jlast = -1;
+    double pref = 0.0, plast = 0.0;
+    for (int g = olo; g < ohi && js < 0; g += 32) {
+        const int j = g + lane;
+        const float sj = j < ohi ? subsum[j] : 0.f;
+        const double in2 = warp_incl_scan_d((double)sj);
+        double ex2v = __shfl_up_sync(full, in2, 1);
+        if (lane == 0) ex2v = 0.0;
+        const unsigned hit = __ballot_sync(full, j < ohi && base + in2 > tau);
+        const unsigned pos = __ballot_sync(full, j < ohi && sj > 0.f);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            js = g + l;
+            pref = base + __shfl_sync(full, ex2v, l);
+        } else if (pos) {
+            const int l = 31 - __clz(pos);
+            jlast = g + l;
+            plast = base + __shfl_sync(full, ex2v, l);
+        }
+        base += __shfl_sync(full, in2, 31);
+    }
+    if (js < 0) {   // rounding between the two levels: take the chunk's last positive sub-tile
+        js = jlast;
+        pref = plast;
+    }
+    if (js < 0) return last_positive<DT, DK, DDT>(c, sm, subsum);
+
+    // level 3: re-read sub-tile js; scan its 32 lanes x 8 elements (the pass's arithmetic)
+    const float tr = (float)(tau - pref);
+    float r[8];
+    int rc = 0;
+    residual8_any<DT, DK, DDT>(c, sm, js, lane, rc, r);
+    const float inc = warp_incl_scan(sum8(r));
+    float exf = __shfl_up_sync(full, inc, 1);
+    if (lane == 0) exf = 0.f;
+    int hitk = -1, lastk = -1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) lastk = r[q] > 0.f ? js * kSub + lane * 8 + q : lastk;
+    const unsigned b2 = __ballot_sync(full, inc > tr);
+    if (b2 != 0) {
+        const int l = __ffs(b2) - 1;
+        if (lane == l) {
+            float part = exf;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                part += r[q];
+                if (hitk < 0 && r[q] > 0.f && part > tr) hitk = js * kSub + lane * 8 + q;
+            }
+            if (hitk < 0) hitk = lastk;
+        }
+        hitk = __shfl_sync(full, hitk, l);
+    }
+    if (hitk < 0) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lastk = max(lastk, shfl_xor(lastk, o));
+        hitk = lastk >= 0 ? lastk : last_positive<DT, DK, DDT>(c, sm, subsum);
+    }
+    return hitk;
+}
+
+// ---- the walk (warp 0) ---------------------------------------------------------------------
+
+struct WalkState {
+    unsigned long long kids;   // children of the current node not tested yet (bit = node)
+    double base, sub;          // point drafts: denominator = base - sub (unnormalised e)
+    double inv_s, inv_sq;      // dense drafts: 1 / S of the node's target and draft rows
+    int node, L, st, await;
+    bool entering, just_summed;
+};
+
+// Advances the walk until it needs a pass over the vocabulary or ends; returns the command.
+// Executed by all lanes of warp 0 with identical state.
+template <int DK>
+__device__ int advance(WalkState &w, Smem &sm, int N) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    if (w.await == CMD_PASS_SR) {
+        w.base = sm.total;
+        w.sub = 0.0;
+        w.just_summed = true;
+    } else if (w.await == CMD_PASS_Z) {
+        const double Z = sm.total;
+        if (lane == 0) {
+            sm.zinv[sm.nlev] = Z > 0.0 ? 1.0 / Z : 0.0;
+            sm.invZ[sm.nlev] = Z > 0.0 ? (float)(1.0 / Z) : 0.f;
+            sm.nlev += 1;
+            sm.pending = 0;
+        }
+        __syncwarp();
+    }
+    w.await = CMD_NONE;
+    for (;;) {
+        if (w.st) return CMD_DONE;
+        if (w.entering) {
+            const unsigned b0 =
+                __ballot_sync(full, lane >= 1 && lane < N && sm.par[lane] == w.node);
+            const unsigned b1 = __ballot_sync(full, lane + 32 < N && sm.par[lane + 32] == w.node);
+            w.kids = ((unsigned long long)b1 << 32) | b0;
+            if (sm.flags[w.node] || (DK != DRAFT_POINT && w.kids && sm.dflags[w.node])) {
+                w.st = SPEC_REQ_BAD_ROW;
+                continue;
+            }
+            w.base = (double)sm.s[w.node];
+            w.sub = 0.0;
+            w.just_summed = false;
+            if (DK != DRAFT_POINT && w.kids) {
+                w.inv_s = 1.0 / (double)sm.s[w.node];
+                w.inv_sq = DK == DRAFT_LOGITS ? 1.0 / (double)sm.sq[w.node] : 1.0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                sm.nR = 0;
+                sm.nlev = 0;
+                sm.pending = 0;
+            }
+            __syncwarp();
+            w.entering = false;
+        }
+        if (w.kids == 0) return CMD_BONUS;
+        if (DK != DRAFT_POINT && sm.pending) {
+            w.await = CMD_PASS_Z;   // normalise the residual the last rejection left
+            return CMD_PASS_Z;
+        }
+        const int c = __ffsll((long long)w.kids) - 1;
+        const double uc = (double)sm.u[c];
+        bool accept;
+        if (DK == DRAFT_POINT) {
+            const int t = sm.tok[c];
+            const int nR = sm.nR;
+            const int r0 = lane < nR ? sm.R[lane] : INT_MAX;
+            const int r1 = lane + 32 < nR ? sm.R[lane + 32] : INT_MAX;
+            const bool dup = __any_sync(full, r0 == t || r1 == t);
+            if (dup) {
+                accept = false;
+            } else {
+                const double denom = w.base - w.sub;
+                if (!w.just_summed && denom < w.base * (1.0 / 16.0)) {
+                    w.await = CMD_PASS_SR;   // most of the mass is rejected: re-sum exactly
+                    return CMD_PASS_SR;
+                }
+                accept = uc * denom < (double)sm.ec[c];   // u < e_t / denom
+            }
+            if (!accept) {
+                if (!dup) {
+                    const int pos = __popc(__ballot_sync(full, r0 < t)) +
+                                    __popc(__ballot_sync(full, r1 < t));
+                    __syncwarp();
+                    if (lane < nR && lane >= pos) sm.R[lane + 1] = r0;
+                    if (lane + 32 < nR && lane + 32 >= pos) sm.R[lane + 33] = r1;
+                    __syncwarp();
+                    if (lane == 0) {
+                        sm.R[pos] = t;
+                        sm.nR = nR + 1;
+                    }
+                    __syncwarp();
+                    w.sub += (double)sm.ec[c];
+                    w.just_summed = false;
+                }
+                w.kids &= w.kids - 1;
+                continue;
+            }
+        } else {
+            const double p = (double)sm.ec[c] * w.inv_s;
+            const double q = (double)sm.eqc[c] * w.inv_sq;
+            double r = p;
+            const int nlev = sm.nlev;
+            for (int l = 0; l < nlev; ++l)
+                if (sm.zinv[l] > 0.0) r = fmax(r - q, 0.0) * sm.zinv[l];
+            accept = uc * q < r;
+            if (!accept) {
+                __syncwarp();
+                if (lane == 0) sm.pending = 1;
+                __syncwarp();
+                w.kids &= w.kids - 1;
+                continue;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) sm.path[w.L] = c;
+        __syncwarp();
+        w.L += 1;
+        w.node = c;
+        w.entering = true;
+    }
+}
+
+template <int DT, int DK, int DDT>
+__device__ __forceinline__ Ctx node_ctx(const SampleWalkParams &P, const Smem &sm, size_t base,
+                                        int nd) {
+    constexpr int kEsz = DT == 1 ? 2 : 4;
+    constexpr int kDEsz = DK == DRAFT_LOGITS ? (DDT == 1 ? 2 : 4) : 4;
+    Ctx c;
+    c.V = (int)P.V;
+    c.k = P.k;
+    c.zrow = reinterpret_cast<const char *>(P.logits) + (base + nd) * (size_t)P.V * kEsz;
+    c.negm = -sm.m[nd];
+    c.invS = 1.f / sm.s[nd];
+    c.zvec = (reinterpret_cast<uintptr_t>(c.zrow) & 15) == 0;
+    c.drow = DK != DRAFT_POINT
+                 ? reinterpret_cast<const char *>(P.draft) + (base + nd) * (size_t)P.V * kDEsz
+                 : nullptr;
+    c.dvec = DK != DRAFT_POINT && (reinterpret_cast<uintptr_t>(c.drow) & 15) == 0;
+    c.negmq = DK == DRAFT_LOGITS ? -sm.mq[nd] : 0.f;
+    c.invSq = DK == DRAFT_LOGITS ? 1.f / sm.sq[nd] : 1.f;
+    c.useq = DK != DRAFT_POINT && (sm.nlev > 0 || sm.pending);
+    return c;
+}
+
+// Point drafts fit 64 registers (2 CTAs per SM); dense drafts keep more live values.
+template <int DT, int DK, int DDT>
+__global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
+    walk_sample_kernel(SampleWalkParams P) {
+    __shared__ Smem sm;
+    extern __shared__ float subsum[];
+    const unsigned full = 0xffffffffu;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const int N = P.N;
+    const size_t base = (size_t)b * N;
+
+    if (tid < N) {
+        sm.par[tid] = P.parent[base + tid];
+        sm.tok[tid] = P.tok[base + tid];
+        sm.flags[tid] = P.flags[base + tid];
+        sm.s[tid] = P.s[base + tid];
+        sm.m[tid] = P.m[base + tid];
+        sm.ec[tid] = tid >= 1 ? P.pc[base + tid] : 0.f;
+        if (DK != DRAFT_POINT) {
+            sm.dflags[tid] = P.dflags[base + tid];
+            sm.eqc[tid] = tid >= 1 ? P.qc[base + tid] : 0.f;
+            if (DK == DRAFT_LOGITS) {
+                sm.sq[tid] = P.sq[base + tid];
+                sm.mq[tid] = P.mq[base + tid];
+            }
+        }
+    }
+    if (tid <= N) sm.u[tid] = P.uniforms[(size_t)b * (N + 1) + tid];
+    if (tid == 0) {
+        sm.nR = 0;
+        sm.nlev = 0;
+        sm.pending = 0;
+        sm.bonus = -1;
+    }
+    __syncthreads();
+
+    WalkState w;
+    w.kids = 0;
+    w.base = w.sub = 0.0;
+    w.inv_s = w.inv_sq = 1.0;
+    w.node = 0;
+    w.L = 0;
+    w.st = 0;
+    w.await = CMD_NONE;
+    w.entering = true;
+    w.just_summed = false;
+    if (warp == 0) {
+        // Request checks in the oracle's order: parents, draft tokens, uniforms.
+        bool bp = false, bt = false, bu = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            if (i < N) {
+                const int p = sm.par[i];
+                bp |= i == 0 ? p != -1 : (p < 0 || p >= i);
+                if (i >= 1) bt |= sm.tok[i] < 0 || sm.tok[i] >= P.V;
+            }
+            const int iu = i + 1;
+            if (iu <= N) bu |= !(sm.u[iu] >= 0.f && sm.u[iu] < 1.f);
+        }
+        w.st = __any_sync(full, bp)   ? SPEC_REQ_BAD_PARENT
+               : __any_sync(full, bt) ? SPEC_REQ_BAD_TOKEN
+               : __any_sync(full, bu) ? SPEC_REQ_BAD_UNIFORM
+                                      : 0;
+    }
+
+    int cmd = CMD_NONE;
+    for (;;) {
+        if (warp == 0) {
+            cmd = advance<DK>(w, sm, N);
+            if (lane == 0) {
+                sm.cmd = cmd;
+                sm.node = w.node;
+                sm.L = w.L;
+                sm.st = w.st;
+            }
+        }
+        __syncthreads();
+        cmd = sm.cmd;
+        if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
+        const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
+        residual_pass<DT, DK, DDT>(c, sm, subsum);
+    }
+
+    if (cmd == CMD_BONUS) {
+        const float ub = sm.u[N];
+        for (int attempt = 0; attempt < 3; ++attempt) {
+            const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
+            residual_pass<DT, DK, DDT>(c, sm, subsum);
+            if (warp == 0) {
+                const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub);
+                if (lane == 0) sm.bonus = v;
+            }
+            __syncthreads();
+            if (sm.bonus >= 0) break;
+            // The residual sums to zero. Dense: the last level is degenerate (target and draft
+            // agree to rounding): keep the previous level. Point: every token with mass was
+            // rejected through rounding: draw from the node's target row.
+            __syncthreads();
+            if (tid == 0) {
+                if (sm.pending) {
+                    sm.pending = 0;
+                } else {
+                    sm.nR = 0;
+                    sm.nlev = 0;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+
+    // Compaction.
+    const int fst = sm.st;
+    const int fL = sm.L;
+    const int fb = sm.bonus;
+    for (int j = tid; j < N; j += kThreads) {
+        int ot = -1, kv = -1;
+        if (fst == 0) {
+            if (j < fL)
+                ot = sm.tok[sm.path[j]];
+            else if (j == fL)
+                ot = fb;
+            if (j == 0)
+                kv = 0;
+            else if (j <= fL)
+                kv = sm.path[j - 1];
+        }
+        P.out.out_tokens[base + j] = ot;
+        P.out.kv_commit[base + j] = kv;
+    }
+    if (tid == 0) {
+        P.out.accept_len[b] = fst ? 0 : fL;
+        P.out.bonus[b] = fst ? -1 : fb;
+        P.out.status[b] = fst;
+    }
+}
+
+template <int DT, int DK, int DDT>
+cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
+    const size_t smem = walk_sample_smem(p.V);
+    walk_sample_kernel<DT, DK, DDT><<<p.B, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t walk_sample_smem(int64_t V) { return sizeof(float) * (size_t)((V + kSub - 1) / kSub); }
+
+cudaError_t launch_walk_sample(const SampleWalkParams &p, cudaStream_t st) {
+    if (p.B <= 0) return cudaSuccess;
+    if (p.draft_kind == DRAFT_POINT) {
+        if (p.dtype == 1) return launch_ws<1, DRAFT_POINT, 0>(p, st);
+        return launch_ws<0, DRAFT_POINT, 0>(p, st);
+    }
+    if (p.draft_kind == DRAFT_PROBS_F32) {
+        if (p.dtype == 1) return launch_ws<1, DRAFT_PROBS_F32, 0>(p, st);
+        return launch_ws<0, DRAFT_PROBS_F32, 0>(p, st);
+    }
+    if (p.dtype == 1) {
+        if (p.draft_dtype == 1) return launch_ws<1, DRAFT_LOGITS, 1>(p, st);
+        return launch_ws<1, DRAFT_LOGITS, 0>(p, st);
+    }
+    if (p.draft_dtype == 1) return launch_ws<0, DRAFT_LOGITS, 1>(p, st);
+    return launch_ws<0, DRAFT_LOGITS, 0>(p, st);
+}
+
+}  // namespace specv
