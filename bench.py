@@ -63,6 +63,16 @@ def barrier(world: int):
         torch.distributed.barrier()
 
 
+def rank_seed(w: W.Workload, rank: int) -> int:
+    """Every rank verifies its own batch of independent requests (weak scaling)."""
+    return w.seed + rank
+
+
+def aggregate_throughput(world: int, draft_nodes_per_rank: int, max_ms: float) -> float:
+    """Whole-job draft nodes/s: all ranks' nodes over the slowest rank's step time."""
+    return world * draft_nodes_per_rank / (max_ms / 1e3)
+
+
 def config_of(w: W.Workload, world: int) -> dict:
     return {"workload": f"{w.name}: B={w.B} N={w.N} V={w.V} {w.dtype} T={w.temperature} "
                         f"point-mass drafts, random tries depth<={w.max_depth} "
@@ -174,6 +184,8 @@ def bench_reference(args):
     if rank != 0:
         return
     w = W.WORKLOADS[WORKLOAD]
+    if args.requests:
+        w = w.scaled(B=args.requests)
     dev = f"cuda:{local}" if torch.cuda.is_available() else "cpu"
     x = W.make(w, device=dev)
     from oracle import oracle as O
@@ -194,7 +206,7 @@ def bench_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w, 1),
+            "data": "synthetic (seeded random tries and N(0,3) logits)", "config": config_of(w, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                              "sample": f"the whole {WORKLOAD} batch per step "
                                        f"({w.B} requests), float64 C oracle"},
@@ -213,7 +225,7 @@ def bench_ours(args):
     w = W.WORKLOADS[WORKLOAD]
     if args.requests:
         w = w.scaled(B=args.requests)
-    x = W.make(w, device=dev, seed=w.seed + rank)
+    x = W.make(w, device=dev, seed=rank_seed(w, rank))
     B, N, V, T = w.B, w.N, w.V, w.temperature
     h = G.Handle(B, N, V, local)
     mask = dict(anc_mask=torch.empty((B, N), dtype=torch.int64, device=dev),
@@ -246,7 +258,7 @@ def bench_ours(args):
     barrier(world)
     ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, world, dev)
-    value = world * w.draft_nodes / (ms / 1e3)
+    value = aggregate_throughput(world, w.draft_nodes, ms)
 
     # dominant kernel: row statistics over all B*N rows
     rs_ms, rs_n = prof["row_stats"]
@@ -297,7 +309,7 @@ def bench_ours(args):
         t2.record(stream)
         torch.cuda.synchronize(dev)
         ems = max_over_ranks(s2.elapsed_time(t2) / k2, world, dev)
-        e2e = {"value": world * w.draft_nodes / (ems / 1e3), "unit": UNIT,
+        e2e = {"value": aggregate_throughput(world, w.draft_nodes, ems), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems, "steps": k2}
 
