@@ -274,6 +274,41 @@ def bench_ours(args):
     kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
                for k, v in prof.items() if v[1]}
 
+    # lazy verification: the same outputs, reading only the rows the walk visits
+    lazy = None
+    if not args.skip_lazy:
+        lout = G.alloc_outputs(B, N, dev)
+
+        def lazy_step():
+            G.spec_build_tree_mask(h, x["parent"], mask["anc_mask"], mask["depth"],
+                                   mask["status"], stream)
+            G.spec_verify_sample_lazy(h, x["logits"], x["draft_token"], x["parent"], T,
+                                      x["uniforms"], lout["accept_len"], lout["out_tokens"],
+                                      lout["kv_commit"], lout["bonus"], lout["status"],
+                                      stream=stream)
+
+        for _ in range(args.warmup):
+            lazy_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        s3, t3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        G.spec_profile_begin(h)
+        s3.record(stream)
+        for _ in range(args.steps):
+            lazy_step()
+        t3.record(stream)
+        torch.cuda.synchronize(dev)
+        lprof = G.spec_profile_end(h)
+        lms = max_over_ranks(s3.elapsed_time(t3) / args.steps, world, dev)
+        al = lout["accept_len"].cpu()
+        same = bool(torch.equal(lout["out_tokens"], out["out_tokens"]))
+        lazy = {"value": aggregate_throughput(world, w.draft_nodes, lms), "unit": UNIT,
+                "ms_per_step": lms,
+                "rows_streamed_per_step": int(al.sum().item()) + 2 * B,
+                "kernels": {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
+                            for k, v in lprof.items() if v[1]},
+                "outputs_equal_eager": same}
+
     # end to end: pinned host inputs -> device, verify, outputs -> pinned host, every step
     e2e = None
     if not args.skip_e2e:
@@ -330,7 +365,7 @@ def bench_ours(args):
                 "config": config_of(w, world),
                 "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
                 "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "lazy": lazy,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
                 "clocks": clocks.summary(), "accept_len_hist": hist}
         print(json.dumps(line), flush=True)
@@ -348,6 +383,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-lazy", action="store_true")
     ap.add_argument("--requests", type=int, default=0,
                     help="requests per rank (default: the workload's 256); for profiling runs")
     args = ap.parse_args(argv)

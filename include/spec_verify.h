@@ -54,7 +54,7 @@ enum {
     SPEC_ERR_WORKSPACE = -4     /* workspace allocation failed */
 };
 
-enum { SPEC_F32 = 0, SPEC_BF16 = 1 };  /* element type of logits / draft logits */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1, SPEC_F16 = 2 };  /* element types (F16: K/V only) */
 
 enum {
     SPEC_DRAFT_POINT = 0,       /* deterministic trie: the draft puts mass 1 on each child */
@@ -68,8 +68,12 @@ enum {
     SPEC_REQ_BAD_TOKEN = 2,     /* a non-root draft token outside [0, V) */
     SPEC_REQ_BAD_ROW = 3,       /* a row the walk needs holds NaN / +inf or is all -inf
                                    (for probabilities: NaN, inf or a negative entry) */
-    SPEC_REQ_BAD_UNIFORM = 4    /* a uniform in slots 1..N is NaN or outside [0, 1) */
+    SPEC_REQ_BAD_UNIFORM = 4,   /* a uniform in slots 1..N is NaN or outside [0, 1) */
+    SPEC_REQ_BAD_SLOT = 5       /* KV commit: a slot maps outside the block table or cache */
 };
+
+enum { SPEC_KV_NHD = 0, SPEC_KV_HND = 1 };  /* paged KV cache layouts */
+enum { SPEC_CACHE_SAME = 0, SPEC_CACHE_FP8_E4M3 = 1, SPEC_CACHE_FP8_E5M2 = 2 };
 
 /* Row-statistics flag bits (spec_row_stats row_flags). */
 enum { SPEC_ROW_NAN = 1, SPEC_ROW_POSINF = 2, SPEC_ROW_ALL_NEGINF = 4 };
@@ -81,7 +85,10 @@ enum {
     SPEC_K_DRAFT_STATS = 2,     /* dense draft rows */
     SPEC_K_WALK_GREEDY = 3,
     SPEC_K_WALK_SAMPLE = 4,
-    SPEC_K_COUNT = 5
+    SPEC_K_LAZY_GREEDY = 5,
+    SPEC_K_LAZY_SAMPLE = 6,
+    SPEC_K_KV_COMMIT = 7,
+    SPEC_K_COUNT = 8
 };
 
 /*
@@ -143,6 +150,55 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
                        int draft_kind, int draft_dtype, float temperature,
                        const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
                        int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream);
+
+/*
+ * Lazy verification: the same operations, arguments, results and status codes as
+ * spec_verify_greedy / spec_verify_sample, but only the rows the walk visits are read (the
+ * accepted path and the stop node: at most depth + 1 rows per request, plus, for dense
+ * drafts, the draft rows of the visited inner nodes), one CTA per request, instead of a
+ * first pass over all B*N rows. EmbodiInfer PR #11 (commit 4b728e2) verifies all trie nodes
+ * in one forward; the walk decides on few of them, so the rows of nodes off the path never
+ * need to be read. Greedy results are bit-identical to the eager call; sampling results can
+ * differ from it only where float32 rounding of a sum decides (the same margin cases as
+ * against the float64 reference). Rows are streamed one after another along the path, so the
+ * latency grows with the accepted length.
+ */
+int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
+                            int64_t V, const int32_t *draft_token, const int32_t *parent,
+                            int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
+                            int32_t *bonus, int32_t *status, void *stream);
+int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
+                            int64_t V, const int32_t *draft_token, const int32_t *parent,
+                            const void *draft, int draft_kind, int draft_dtype, float temperature,
+                            const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
+                            int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream);
+
+/*
+ * KV commit after verification (IluvatarLabs/vllm PR #3, commit_draft_kernel: the K/V of
+ * accepted draft tokens are copied into the paged cache, NHD or HND, fp16/bf16/fp32 sources,
+ * a cache of the source type or fp8 with a scale, rejected entries skipped; EmbodiInfer PR #11,
+ * commits 938fe7b and 41dcd00: only the new tokens are committed).
+ *   src_k, src_v    [B, N, H, D] of src_dtype (SPEC_F32 / SPEC_BF16 / SPEC_F16): the K/V the
+ *                   verify forward produced for every tree node;
+ *   kv_commit, accept_len   outputs of a verify call ([B, N] and [B]);
+ *   cache_k, cache_v        paged caches, layout SPEC_KV_NHD [num_blocks, block_size, H, D] or
+ *                   SPEC_KV_HND [num_blocks, H, block_size, D]; element type: the source type
+ *                   (SPEC_CACHE_SAME) or one byte of fp8 (SPEC_CACHE_FP8_E4M3 / _E5M2);
+ *   block_table     int32 [B, max_blocks]: cache block of each block_size tokens of request b;
+ *   seq_pos         int32 [B]: sequence position of slot 0 (the root);
+ *   k_scale, v_scale        device float scalars for fp8 caches (NULL = 1): the cache stores
+ *                   the fp8 rounding (nearest, ties to even, saturated) of x / scale;
+ *   commit_status   int32 [B] (may be NULL): SPEC_REQ_BAD_SLOT if a slot's position or block
+ *                   falls outside the table or the cache (that slot is skipped), else 0.
+ * Slot j of request b (j = 0..accept_len[b]) is written at position seq_pos[b] + j. Requests
+ * whose kv_commit[b][0] is negative (verification failed) write nothing.
+ */
+int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_dtype, int B,
+                   int N, int H, int D, const int32_t *kv_commit, const int32_t *accept_len,
+                   void *cache_k, void *cache_v, int cache_kind, int layout, int block_size,
+                   int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                   const int32_t *seq_pos, const float *k_scale, const float *v_scale,
+                   int32_t *commit_status, void *stream);
 
 /*
  * The vocabulary-streaming row statistics on their own (the first stage of both verify

@@ -163,8 +163,10 @@ int oracle_row_softmax(const void *row, int dtype, int64_t V, double T, double *
 
 /* InvCDF(r, u): with S = sum r and tau = u*S, the smallest v whose running sum exceeds
  * tau; if rounding leaves none, the largest v with r[v] > 0. The margin is the distance of
- * tau to the nearer end of the chosen interval, over S (0 on the fallback). */
-static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin) {
+ * tau to the nearer end of the chosen interval, over S (0 on the fallback). *alt is the token
+ * with r > 0 on the other side of that nearer end (v itself if there is none): the draw an
+ * arithmetic that rounds the running sums differently may make when the margin is tiny. */
+static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin, int64_t *alt) {
     double S = 0.0;
     for (int64_t v = 0; v < V; v++) S += r[v];
     double tau = u * S;
@@ -175,17 +177,36 @@ static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin) {
         if (C > tau) {
             double a = C - tau, b = tau - Cprev;
             *margin = (a < b ? a : b) / S;
+            *alt = v;
+            if (a < b) {
+                for (int64_t w = v + 1; w < V; w++)
+                    if (r[w] > 0) {
+                        *alt = w;
+                        break;
+                    }
+            } else {
+                for (int64_t w = v - 1; w >= 0; w--)
+                    if (r[w] > 0) {
+                        *alt = w;
+                        break;
+                    }
+            }
             return v;
         }
     }
     *margin = 0.0;
     for (int64_t v = V - 1; v >= 0; v--)
-        if (r[v] > 0) return v;
+        if (r[v] > 0) {
+            *alt = v;
+            return v;
+        }
+    *alt = V - 1;
     return V - 1;
 }
 
 int64_t oracle_inv_cdf(const double *r, int64_t V, double u, double *margin) {
-    return inv_cdf(r, V, u, margin);
+    int64_t alt;
+    return inv_cdf(r, V, u, margin, &alt);
 }
 
 /* ---- per-request outputs ------------------------------------------------------------------ */
@@ -301,7 +322,8 @@ typedef struct {
  * unused; the test is strict (u < rhat). */
 static int32_t sample_point(const void *logits, int dtype, int b, int N, int64_t V, double T,
                             const int32_t *tok, const int32_t *par, const float *u,
-                            scratch s, int *path, int *L_out, double *dmargin, double *cmargin) {
+                            scratch s, int *path, int *L_out, double *dmargin, double *cmargin,
+                            int32_t *calt) {
     int node = 0, L = 0;
     double *p = s.p, *r = s.r;
     char *inR = (char *)s.tmp; /* V bytes */
@@ -335,8 +357,10 @@ static int32_t sample_point(const void *logits, int dtype, int b, int N, int64_t
     }
     for (int64_t v = 0; v < V; v++) r[v] = inR[v] ? 0.0 : p[v];
     double cm;
-    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm);
+    int64_t alt;
+    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt);
     *cmargin = cm;
+    *calt = (int32_t)alt;
     *L_out = L;
     return (int32_t)bonus;
 }
@@ -372,7 +396,7 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
                             const int32_t *tok, const int32_t *par, const void *draft,
                             int draft_kind, int draft_dtype, const float *u, scratch s,
                             int *path, int *L_out, double *dmargin, double *cmargin,
-                            int32_t *degenerate) {
+                            int32_t *degenerate, int32_t *calt) {
     int node = 0, L = 0;
     double *p = s.p, *r = s.r, *q = s.q;
     for (;;) {
@@ -417,8 +441,10 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
         node = next;
     }
     double cm;
-    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm);
+    int64_t alt;
+    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt);
     *cmargin = cm;
+    *calt = (int32_t)alt;
     *L_out = L;
     return (int32_t)bonus;
 }
@@ -427,14 +453,15 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
  * in [0, 1) or the request fails with status 4 (READING: checked before the walk, whether or
  * not the walk consumes the slot). decision_margin[b] is the smallest |u - r(x)/q(x)| over
  * the tests taken (= |u*q - r|/q, never below |u*q - r| as q <= 1; +inf if no test),
- * cdf_margin[b] the bonus draw's margin, degenerate[b] the number of degenerate dense
- * residuals. */
+ * cdf_margin[b] the bonus draw's margin, cdf_alt[b] the token across the nearer boundary of
+ * the drawn interval, degenerate[b] the number of degenerate dense residuals. */
 int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
                          const int32_t *draft_token, const int32_t *parent, const void *draft,
                          int draft_kind, int draft_dtype, double T, const float *uniforms,
                          int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
                          int32_t *bonus, int32_t *status, double *decision_margin,
-                         double *cdf_margin, int32_t *degenerate, int nthreads) {
+                         double *cdf_margin, int32_t *cdf_alt, int32_t *degenerate,
+                         int nthreads) {
     if (B < 0 || N < 1 || N > 64 || V < 1 || (dtype != OR_F32 && dtype != OR_BF16)) return -1;
     if (!(T >= 0.0) || isinf(T)) return -1;
     if (draft_kind != OR_DRAFT_POINT && draft_kind != OR_DRAFT_PROBS_F32 &&
@@ -452,6 +479,7 @@ int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
         const float *u = uniforms + (size_t)b * (N + 1);
         decision_margin[b] = INFINITY;
         cdf_margin[b] = INFINITY;
+        cdf_alt[b] = -1;
         degenerate[b] = 0;
         if (T == 0.0) {
             greedy_one(logits, dtype, b, N, V, tok, par, o);
@@ -474,11 +502,11 @@ int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
         int32_t res;
         if (draft_kind == OR_DRAFT_POINT)
             res = sample_point(logits, dtype, b, N, V, T, tok, par, u, s, path, &L,
-                               &decision_margin[b], &cdf_margin[b]);
+                               &decision_margin[b], &cdf_margin[b], &cdf_alt[b]);
         else
             res = sample_dense(logits, dtype, b, N, V, T, tok, par, draft, draft_kind,
                                draft_dtype, u, s, path, &L, &decision_margin[b],
-                               &cdf_margin[b], &degenerate[b]);
+                               &cdf_margin[b], &degenerate[b], &cdf_alt[b]);
         if (res < 0)
             write_failed(o, b, N, -res);
         else

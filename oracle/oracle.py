@@ -59,7 +59,7 @@ class Oracle:
         lib.oracle_inv_cdf.restype = i64
         lib.oracle_verify_greedy.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, P, P, i32]
         lib.oracle_verify_sample.argtypes = [P, i32, i32, i32, i64, P, P, P, i32, i32, f64,
-                                             P, P, P, P, P, P, P, P, P, i32]
+                                             P, P, P, P, P, P, P, P, P, P, i32]
         lib.oracle_max_threads.restype = i32
         self.lib = lib
         self.path = path
@@ -146,16 +146,17 @@ class Oracle:
         al, ot, kv, bo, st = self._outputs(B, N)
         dm = np.zeros(B, np.float64)
         cm = np.zeros(B, np.float64)
+        ca = np.zeros(B, np.int32)
         dg = np.zeros(B, np.int32)
         rc = self.lib.oracle_verify_sample(_ptr(logits), _dtype_code(logits), B, N, V,
                                            _ptr(tok), _ptr(par), _ptr(draft), int(draft_kind),
                                            ddt, float(temperature), _ptr(u), _ptr(al), _ptr(ot),
                                            _ptr(kv), _ptr(bo), _ptr(st), _ptr(dm), _ptr(cm),
-                                           _ptr(dg), int(nthreads))
+                                           _ptr(ca), _ptr(dg), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_verify_sample rejected its arguments")
         return dict(accept_len=al, out_tokens=ot, kv_commit=kv, bonus=bo, status=st,
-                    decision_margin=dm, cdf_margin=cm, degenerate=dg)
+                    decision_margin=dm, cdf_margin=cm, cdf_alt=ca, degenerate=dg)
 
 
 _default: Oracle | None = None

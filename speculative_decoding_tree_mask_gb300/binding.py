@@ -21,7 +21,12 @@ SPEC_DRAFT_POINT, SPEC_DRAFT_PROBS_F32, SPEC_DRAFT_LOGITS = 0, 1, 2
 SPEC_REQ_OK, SPEC_REQ_BAD_PARENT, SPEC_REQ_BAD_TOKEN, SPEC_REQ_BAD_ROW, SPEC_REQ_BAD_UNIFORM = \
     0, 1, 2, 3, 4
 SPEC_ROW_NAN, SPEC_ROW_POSINF, SPEC_ROW_ALL_NEGINF = 1, 2, 4
-KERNEL_CLASSES = ("tree_mask", "row_stats", "draft_stats", "walk_greedy", "walk_sample")
+KERNEL_CLASSES = ("tree_mask", "row_stats", "draft_stats", "walk_greedy", "walk_sample",
+                  "lazy_greedy", "lazy_sample", "kv_commit")
+SPEC_F16 = 2
+SPEC_REQ_BAD_SLOT = 5
+SPEC_KV_NHD, SPEC_KV_HND = 0, 1
+SPEC_CACHE_SAME, SPEC_CACHE_FP8_E4M3, SPEC_CACHE_FP8_E5M2 = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +56,10 @@ def load() -> ctypes.CDLL:
             lib.spec_verify_sample.argtypes = [P, P, i32, i32, i32, i64, P, P, P, i32, i32, f32,
                                                P, P, P, P, P, P, P]
             lib.spec_row_stats.argtypes = [P, P, i32, i32, i32, i64, f32, P, P, P, P, P, P, P, P]
+            lib.spec_verify_greedy_lazy.argtypes = lib.spec_verify_greedy.argtypes
+            lib.spec_kv_commit.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32,
+                                           i32, i32, i64, P, i32, P, P, P, P, P]
+            lib.spec_verify_sample_lazy.argtypes = lib.spec_verify_sample.argtypes
             lib.spec_profile_begin.argtypes = [P]
             lib.spec_profile_end.argtypes = [P, P, P]
             lib.spec_error_string.argtypes = [i32]
@@ -173,6 +182,35 @@ def spec_verify_sample(h: Handle, logits, draft_token, parent, temperature: floa
         _stream(stream, logits.device)), "spec_verify_sample")
 
 
+def spec_verify_greedy_lazy(h: Handle, logits, draft_token, parent, accept_len, out_tokens,
+                            kv_commit, bonus, status, stream=None):
+    """Greedy verification reading only the rows on the accepted path."""
+    B, N, V = logits.shape
+    _check(load().spec_verify_greedy_lazy(
+        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
+        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
+        _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
+        _stream(stream, logits.device)), "spec_verify_greedy_lazy")
+
+
+def spec_verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature: float, uniforms,
+                            accept_len, out_tokens, kv_commit, bonus, status, draft=None,
+                            draft_kind: int = SPEC_DRAFT_POINT, stream=None):
+    """Sampling verification reading only the rows the walk visits."""
+    B, N, V = logits.shape
+    ddt = 0
+    if draft is not None and draft_kind == SPEC_DRAFT_LOGITS:
+        ddt = _dtype_code(draft)
+    if draft is not None and draft_kind == SPEC_DRAFT_PROBS_F32 and draft.dtype != torch.float32:
+        raise TypeError("draft probabilities must be float32")
+    _check(load().spec_verify_sample_lazy(
+        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
+        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")), _ptr(draft),
+        int(draft_kind), ddt, float(temperature), _ptr(uniforms), _ptr(accept_len),
+        _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
+        _stream(stream, logits.device)), "spec_verify_sample_lazy")
+
+
 def spec_row_stats(h: Handle, logits, N: int, temperature: float, row_max, row_sum, row_argmax,
                    row_flags, draft_token=None, parent=None, child_prob=None, stream=None):
     """logits [rows, V] (or [B, N, V]) -> per-row max, sum, argmax, flags; optional gather of
@@ -183,6 +221,31 @@ def spec_row_stats(h: Handle, logits, N: int, temperature: float, row_max, row_s
         h.ptr, _ptr(logits), _dtype_code(logits), rows, int(N), V, float(temperature),
         _ptr(draft_token), _ptr(parent), _ptr(row_max), _ptr(row_sum), _ptr(row_argmax),
         _ptr(row_flags), _ptr(child_prob), _stream(stream, logits.device)), "spec_row_stats")
+
+
+def _kv_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return SPEC_F16
+    return _dtype_code(t)
+
+
+def spec_kv_commit(h: Handle, src_k, src_v, kv_commit, accept_len, cache_k, cache_v, layout: int,
+                   block_table, seq_pos, cache_kind: int = SPEC_CACHE_SAME, k_scale=None,
+                   v_scale=None, commit_status=None, stream=None):
+    """Copy the K/V of the root and the accepted nodes ([B, N, H, D]) into a paged cache
+    (NHD [blocks, block_size, H, D] or HND [blocks, H, block_size, D]); fp8 caches are uint8."""
+    B, N, H, D = src_k.shape
+    if layout == SPEC_KV_NHD:
+        num_blocks, block_size = cache_k.shape[0], cache_k.shape[1]
+    else:
+        num_blocks, block_size = cache_k.shape[0], cache_k.shape[2]
+    _check(load().spec_kv_commit(
+        h.ptr, _ptr(src_k), _ptr(src_v), _kv_dtype(src_k), B, N, H, D,
+        _ptr(_i32(kv_commit, "kv_commit")), _ptr(_i32(accept_len, "accept_len")), _ptr(cache_k),
+        _ptr(cache_v), int(cache_kind), int(layout), int(block_size), int(num_blocks),
+        _ptr(_i32(block_table, "block_table")), int(block_table.shape[1]),
+        _ptr(_i32(seq_pos, "seq_pos")), _ptr(k_scale), _ptr(v_scale), _ptr(commit_status),
+        _stream(stream, src_k.device)), "spec_kv_commit")
 
 
 def spec_profile_begin(h: Handle):
@@ -222,6 +285,25 @@ def verify_sample(h: Handle, logits, draft_token, parent, temperature, uniforms,
     spec_verify_sample(h, logits, draft_token, parent, temperature, uniforms, out["accept_len"],
                        out["out_tokens"], out["kv_commit"], out["bonus"], out["status"], draft,
                        draft_kind, stream)
+    return out
+
+
+def verify_greedy_lazy(h: Handle, logits, draft_token, parent, out: dict | None = None,
+                       stream=None) -> dict:
+    B, N, _ = logits.shape
+    out = out or alloc_outputs(B, N, logits.device)
+    spec_verify_greedy_lazy(h, logits, draft_token, parent, out["accept_len"], out["out_tokens"],
+                            out["kv_commit"], out["bonus"], out["status"], stream)
+    return out
+
+
+def verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature, uniforms, draft=None,
+                       draft_kind=SPEC_DRAFT_POINT, out: dict | None = None, stream=None) -> dict:
+    B, N, _ = logits.shape
+    out = out or alloc_outputs(B, N, logits.device)
+    spec_verify_sample_lazy(h, logits, draft_token, parent, temperature, uniforms,
+                            out["accept_len"], out["out_tokens"], out["kv_commit"], out["bonus"],
+                            out["status"], draft, draft_kind, stream)
     return out
 
 

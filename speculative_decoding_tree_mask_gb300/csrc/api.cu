@@ -1,6 +1,7 @@
 // C ABI of the verification library (declared in include/spec_verify.h): handle and
 // workspace, host-side argument checks, kernel orchestration and per-kernel timing.
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -319,6 +320,138 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     wp.dflags = h->dflags;
     wp.out = out;
     return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
+}
+
+int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
+                            int64_t V, const int32_t *draft_token, const int32_t *parent,
+                            int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
+                            int32_t *bonus, int32_t *status, void *stream) {
+    int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
+                          out_tokens, kv_commit, bonus, status);
+    if (rc != SPEC_OK || B == 0) return rc;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    LazyGreedyParams lp;
+    lp.B = B;
+    lp.N = N;
+    lp.V = V;
+    lp.dtype = dtype;
+    lp.logits = logits;
+    lp.parent = parent;
+    lp.tok = draft_token;
+    lp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
+    return timed(h, SPEC_K_LAZY_GREEDY, st, [&] { return launch_lazy_greedy(lp, st); });
+}
+
+int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
+                            int64_t V, const int32_t *draft_token, const int32_t *parent,
+                            const void *draft, int draft_kind, int draft_dtype, float temperature,
+                            const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
+                            int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream) {
+    int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
+                          out_tokens, kv_commit, bonus, status);
+    if (rc != SPEC_OK) return rc;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return SPEC_ERR_ARG;
+    const float k = temperature > 0.f ? kLog2eF / temperature : 0.f;
+    if (temperature > 0.f && !std::isfinite(k)) return SPEC_ERR_ARG;
+    if (draft_kind != SPEC_DRAFT_POINT && draft_kind != SPEC_DRAFT_PROBS_F32 &&
+        draft_kind != SPEC_DRAFT_LOGITS)
+        return SPEC_ERR_ARG;
+    if (draft_kind == SPEC_DRAFT_LOGITS && draft_dtype != SPEC_F32 && draft_dtype != SPEC_BF16)
+        return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    if (temperature == 0.f)
+        return spec_verify_greedy_lazy(h, logits, dtype, B, N, V, draft_token, parent,
+                                       accept_len, out_tokens, kv_commit, bonus, status, stream);
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_ARG;
+    if (draft_kind != SPEC_DRAFT_POINT) {
+        if (!draft) return SPEC_ERR_ARG;
+        const size_t de = draft_kind == SPEC_DRAFT_LOGITS ? esize(draft_dtype) : 4;
+        if (!aligned(draft, de)) return SPEC_ERR_ARG;
+    }
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SampleWalkParams wp{};
+    wp.B = B;
+    wp.N = N;
+    wp.V = V;
+    wp.dtype = dtype;
+    wp.logits = logits;
+    wp.parent = parent;
+    wp.tok = draft_token;
+    wp.uniforms = uniforms;
+    wp.k = k;
+    wp.draft_kind = draft_kind;
+    wp.draft_dtype = draft_dtype;
+    wp.draft = draft;
+    wp.lazy = 1;
+    wp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
+    return timed(h, SPEC_K_LAZY_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
+}
+
+int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_dtype, int B,
+                   int N, int H, int D, const int32_t *kv_commit, const int32_t *accept_len,
+                   void *cache_k, void *cache_v, int cache_kind, int layout, int block_size,
+                   int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                   const int32_t *seq_pos, const float *k_scale, const float *v_scale,
+                   int32_t *commit_status, void *stream) {
+    if (!h) return SPEC_ERR_ARG;
+    if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
+    if (H < 1 || D < 1 || (int64_t)H * D > (int64_t(1) << 24)) return SPEC_ERR_ARG;
+    if (src_dtype != SPEC_F32 && src_dtype != SPEC_BF16 && src_dtype != SPEC_F16)
+        return SPEC_ERR_ARG;
+    if (cache_kind != SPEC_CACHE_SAME && cache_kind != SPEC_CACHE_FP8_E4M3 &&
+        cache_kind != SPEC_CACHE_FP8_E5M2)
+        return SPEC_ERR_ARG;
+    if (layout != SPEC_KV_NHD && layout != SPEC_KV_HND) return SPEC_ERR_ARG;
+    if (block_size < 1 || num_blocks < 1 || num_blocks > INT32_MAX || max_blocks < 1)
+        return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!src_k || !src_v || !kv_commit || !accept_len || !cache_k || !cache_v || !block_table ||
+        !seq_pos)
+        return SPEC_ERR_ARG;
+    const size_t se = src_dtype == SPEC_F32 ? 4 : 2;
+    const size_t ce = cache_kind == SPEC_CACHE_SAME ? se : 1;
+    if (!aligned(src_k, se) || !aligned(src_v, se) || !aligned(cache_k, ce) ||
+        !aligned(cache_v, ce))
+        return SPEC_ERR_ARG;
+    const void *ints[] = {kv_commit, accept_len, block_table, seq_pos};
+    for (const void *p : ints)
+        if (!aligned(p, 4)) return SPEC_ERR_ARG;
+    if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)) ||
+        (commit_status && !aligned(commit_status, 4)))
+        return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    KvCommitParams kp;
+    kp.src_k = src_k;
+    kp.src_v = src_v;
+    kp.src_dtype = src_dtype;
+    kp.B = B;
+    kp.N = N;
+    kp.H = H;
+    kp.D = D;
+    kp.kv_commit = kv_commit;
+    kp.accept_len = accept_len;
+    kp.cache_k = cache_k;
+    kp.cache_v = cache_v;
+    kp.cache_kind = cache_kind;
+    kp.layout = layout;
+    kp.block_size = block_size;
+    kp.num_blocks = num_blocks;
+    kp.block_table = block_table;
+    kp.max_blocks = max_blocks;
+    kp.seq_pos = seq_pos;
+    kp.k_scale = k_scale;
+    kp.v_scale = v_scale;
+    kp.status = commit_status;
+    // 8 elements per thread step: rows of D elements and 16-byte aligned bases.
+    const bool vec = D % 8 == 0 && aligned(src_k, 16) && aligned(src_v, 16) &&
+                     aligned(cache_k, 16) && aligned(cache_v, 16);
+    return timed(h, SPEC_K_KV_COMMIT, st, [&] { return launch_kv_commit(kp, vec, st); });
 }
 
 int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N, int64_t V,

@@ -16,149 +16,18 @@
 
 #include <cfloat>
 
+#include "row_pass.cuh"
 #include "spec_device.cuh"
 #include "spec_internal.h"
 
 namespace specv {
 namespace {
 
+using namespace rowpass;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
-
-enum { F_NAN = 1, F_POSINF = 2, F_ALLNEG = 4 };
-
-struct Acc {
-    float m;      // running max (never NaN)
-    float negm;   // -m once m is finite, else 0
-    float s0, s1; // partial sums of 2^((x - m) k)
-    int arg;      // lowest index attaining m (kNone before any non -inf element)
-    int flags;
-};
-
-template <int MODE>
-__device__ __forceinline__ void raise_max(Acc &a, float v, float k) {
-    if (MODE == ROW_SAMPLE) {
-        if (a.m == -INFINITY) {
-            a.s0 = 0.f;
-            a.s1 = 0.f;
-        } else {
-            const float f = ex2((a.m - v) * k);
-            a.s0 *= f;
-            a.s1 *= f;
-        }
-    }
-    a.m = v;
-    a.negm = -v;
-}
-
-// One scalar element (head / tail of a misaligned row).
-template <int MODE>
-__device__ __forceinline__ void proc_scalar(Acc &a, float x, int idx, float k) {
-    if (MODE == ROW_PROBS) {
-        if (!(x >= 0.f && x < INFINITY)) a.flags |= F_NAN;
-        return;
-    }
-    if (x != x) {
-        a.flags |= F_NAN;
-    } else if (x > a.m) {
-        raise_max<MODE>(a, x, k);
-        a.arg = idx;
-    }
-    if (MODE == ROW_SAMPLE) a.s0 += ex2((x + a.negm) * k);
-}
-
-// Eight bf16 values (one 16-byte vector) starting at element e0.
-template <int MODE>
-__device__ __forceinline__ void proc_bf16(Acc &a, const uint4 w, int e0, float k) {
-    const uint32_t mm = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
-    const float vmax = fmax_nan(bf_lo(mm), bf_hi(mm));
-    if (!(vmax <= a.m)) {
-        if (vmax != vmax) {
-            a.flags |= F_NAN;
-        } else {
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            int j = 7;
-#pragma unroll
-            for (int q = 3; q >= 0; --q) {
-                if (bf_hi(ws[q]) == vmax) j = 2 * q + 1;
-                if (bf_lo(ws[q]) == vmax) j = 2 * q;
-            }
-            raise_max<MODE>(a, vmax, k);
-            a.arg = e0 + j;
-        }
-    }
-    if (MODE == ROW_SAMPLE) {
-        float d0, d1, d2, d3, d4, d5, d6, d7;
-        bf_add2(w.x, a.negm, d0, d1);
-        bf_add2(w.y, a.negm, d2, d3);
-        bf_add2(w.z, a.negm, d4, d5);
-        bf_add2(w.w, a.negm, d6, d7);
-        a.s0 += ex2(d0 * k) + ex2(d2 * k) + (ex2(d4 * k) + ex2(d6 * k));
-        a.s1 += ex2(d1 * k) + ex2(d3 * k) + (ex2(d5 * k) + ex2(d7 * k));
-    }
-}
-
-// Four f32 values (one 16-byte vector) starting at element e0.
-template <int MODE>
-__device__ __forceinline__ void proc_f32(Acc &a, const uint4 w, int e0, float k) {
-    const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                        __uint_as_float(w.w)};
-    if (MODE == ROW_PROBS) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (!(x[q] >= 0.f && x[q] < INFINITY)) a.flags |= F_NAN;
-        return;
-    }
-    const float vmax = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
-    if (!(vmax <= a.m)) {
-        if (vmax != vmax) {
-            a.flags |= F_NAN;
-        } else {
-            int j = 3;
-#pragma unroll
-            for (int q = 2; q >= 0; --q)
-                if (x[q] == vmax) j = q;
-            raise_max<MODE>(a, vmax, k);
-            a.arg = e0 + j;
-        }
-    }
-    if (MODE == ROW_SAMPLE) {
-        a.s0 += ex2((x[0] + a.negm) * k) + ex2((x[2] + a.negm) * k);
-        a.s1 += ex2((x[1] + a.negm) * k) + ex2((x[3] + a.negm) * k);
-    }
-}
-
-struct Part {
-    float m, s;
-    int arg, flags;
-};
-
-template <int MODE>
-__device__ __forceinline__ Part merge(Part x, Part y, float k) {
-    Part r;
-    r.m = fmaxf(x.m, y.m);
-    r.flags = x.flags | y.flags;
-    r.arg = x.m > y.m ? x.arg : (y.m > x.m ? y.arg : min(x.arg, y.arg));
-    r.s = 0.f;
-    if (MODE == ROW_SAMPLE && r.m != -INFINITY)
-        r.s = x.s * ex2((x.m - r.m) * k) + y.s * ex2((y.m - r.m) * k);
-    return r;
-}
-
-template <int MODE>
-__device__ __forceinline__ Part warp_merge(Part p, float k) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Part q;
-        q.m = shfl_xor(p.m, o);
-        q.s = shfl_xor(p.s, o);
-        q.arg = shfl_xor(p.arg, o);
-        q.flags = shfl_xor(p.flags, o);
-        p = merge<MODE>(p, q, k);
-    }
-    return p;
-}
 
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P) {

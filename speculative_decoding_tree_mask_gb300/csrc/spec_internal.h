@@ -54,6 +54,18 @@ struct GreedyWalkParams {
 
 cudaError_t launch_walk_greedy(const GreedyWalkParams &p, cudaStream_t st);
 
+// Greedy verification reading only the rows on the accepted path (one CTA per request).
+struct LazyGreedyParams {
+    int B, N;
+    int64_t V;
+    int dtype;
+    const void *logits;
+    const int32_t *parent, *tok;
+    WalkOutputs out;
+};
+
+cudaError_t launch_lazy_greedy(const LazyGreedyParams &p, cudaStream_t st);
+
 struct SampleWalkParams {
     int B, N;
     int64_t V;
@@ -70,8 +82,29 @@ struct SampleWalkParams {
     const void *draft;
     const float *mq, *sq, *qc;
     const int32_t *dflags;
+    int lazy;                     // 1: no row statistics precomputed; stream visited rows only
     WalkOutputs out;
 };
+
+// KV commit of the accepted path into a paged cache (see spec_kv_commit).
+struct KvCommitParams {
+    const void *src_k, *src_v;
+    int src_dtype;                // 0 f32, 1 bf16, 2 f16
+    int B, N, H, D;
+    const int32_t *kv_commit, *accept_len;
+    void *cache_k, *cache_v;
+    int cache_kind;               // 0 source type, 1 fp8 e4m3, 2 fp8 e5m2
+    int layout;                   // 0 NHD, 1 HND
+    int block_size;
+    int64_t num_blocks;
+    const int32_t *block_table;
+    int max_blocks;
+    const int32_t *seq_pos;
+    const float *k_scale, *v_scale;
+    int32_t *status;
+};
+
+cudaError_t launch_kv_commit(const KvCommitParams &p, bool vec, cudaStream_t st);
 
 // Dynamic shared memory the sampling walk needs for vocabulary size V.
 size_t walk_sample_smem(int64_t V);

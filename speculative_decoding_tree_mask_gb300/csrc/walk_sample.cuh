@@ -1,4 +1,5 @@
-// Sampling tree walk, inverse-CDF bonus draw and accepted-path compaction.
+// Sampling tree walk, inverse-CDF bonus draw and accepted-path compaction (kernel templates;
+// instantiated by walk_sample_point.cu and walk_sample_dense.cu).
 //
 // EmbodiInfer PR #11 "perf(activevln): grammar-trie speculation and lossless throughput",
 // commit 4b728e2: sampling uses standard (SpecInfer-style) rejection sampling against the
@@ -26,8 +27,11 @@
 // per SM: 128 KiB of each SM's loads in flight); sums use compensated float32, and the
 // float64 pipe (slow on this part) only sees a handful of operations per decision.
 
+#pragma once
+
 #include <climits>
 
+#include "row_pass.cuh"
 #include "spec_device.cuh"
 #include "spec_internal.h"
 
@@ -38,7 +42,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSub = 256;   // elements per sub-tile: 32 lanes x 8
 
-enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z };
+enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z, CMD_STATS };
 
 struct Smem {
     int par[kMaxN], tok[kMaxN], flags[kMaxN], dflags[kMaxN];
@@ -54,6 +58,8 @@ struct Smem {
     int cmd, node, L, st, bonus;
     double total;
     double wtot[kWarps];
+    int haskids;                       // lazy statistics: the node has children
+    rowpass::Part part[kWarps], part_out;
 };
 
 struct Ctx {
@@ -374,11 +380,12 @@ struct WalkState {
     double inv_s, inv_sq;      // dense drafts: 1 / S of the node's target and draft rows
     int node, L, st, await;
     bool entering, just_summed;
+    bool stats_ready;          // lazy walks: the current node's statistics are in shared memory
 };
 
 // Advances the walk until it needs a pass over the vocabulary or ends; returns the command.
 // Executed by all lanes of warp 0 with identical state.
-template <int DK>
+template <int DK, bool LAZY>
 __device__ int advance(WalkState &w, Smem &sm, int N) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -386,6 +393,8 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
         w.base = sm.total;
         w.sub = 0.0;
         w.just_summed = true;
+    } else if (w.await == CMD_STATS) {
+        w.stats_ready = true;
     } else if (w.await == CMD_PASS_Z) {
         const double Z = sm.total;
         if (lane == 0) {
@@ -404,6 +413,10 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
                 __ballot_sync(full, lane >= 1 && lane < N && sm.par[lane] == w.node);
             const unsigned b1 = __ballot_sync(full, lane + 32 < N && sm.par[lane + 32] == w.node);
             w.kids = ((unsigned long long)b1 << 32) | b0;
+            if (LAZY && !w.stats_ready) {
+                w.await = CMD_STATS;   // stream the node's row(s) first
+                return CMD_STATS;
+            }
             if (sm.flags[w.node] || (DK != DRAFT_POINT && w.kids && sm.dflags[w.node])) {
                 w.st = SPEC_REQ_BAD_ROW;
                 continue;
@@ -489,7 +502,78 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
         w.L += 1;
         w.node = c;
         w.entering = true;
+        w.stats_ready = false;
     }
+}
+
+// Lazy walks: the statistics of the node's target row (and, for dense drafts of an inner
+// node, of its draft row) with the same per-element arithmetic as the row-statistics
+// kernel, plus e_t at the children's tokens. All threads call it; it ends synchronised.
+template <int DT, int DK, int DDT>
+__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd) {
+    constexpr int kEsz = DT == 1 ? 2 : 4;
+    constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
+    constexpr int kDEsz = kDDT == 1 ? 2 : 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int N = P.N;
+    const int64_t V = P.V;
+    const float k = P.k;
+    const char *zrow = reinterpret_cast<const char *>(P.logits) + (base + nd) * (size_t)V * kEsz;
+    int cc[2] = {-1, -1};
+    float zc[2] = {0.f, 0.f};
+    if (warp == 0) {
+        bool any = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = lane + 32 * h;
+            if (c >= 1 && c < N && sm.par[c] == nd) {
+                any = true;
+                cc[h] = c;
+                zc[h] = load_elem<DT>(zrow, sm.tok[c]);   // tokens were validated
+            }
+        }
+        const bool kids = __any_sync(0xffffffffu, any);
+        if (lane == 0) sm.haskids = kids;
+    }
+    const rowpass::Part p =
+        rowpass::cta_row_stats<DT, ROW_SAMPLE, kThreads, 4>(zrow, V, k, sm.part, &sm.part_out);
+    if (warp == 0) {
+        const float negm = p.m == -INFINITY ? 0.f : -p.m;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (cc[h] >= 0) sm.ec[cc[h]] = ex2((zc[h] + negm) * k);
+        if (lane == 0) {
+            sm.m[nd] = p.m;
+            sm.s[nd] = p.s;
+            sm.flags[nd] = p.flags;
+        }
+    }
+    if (DK != DRAFT_POINT && sm.haskids) {
+        const char *drow =
+            reinterpret_cast<const char *>(P.draft) + (base + nd) * (size_t)V * kDEsz;
+        float dc[2] = {0.f, 0.f};
+        if (warp == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (cc[h] >= 0) dc[h] = load_elem<kDDT>(drow, sm.tok[cc[h]]);
+        }
+        const rowpass::Part q =
+            rowpass::cta_row_stats<kDDT, DK == DRAFT_LOGITS ? ROW_SAMPLE : ROW_PROBS, kThreads,
+                                   4>(drow, V, k, sm.part, &sm.part_out);
+        if (warp == 0) {
+            const float negmq = q.m == -INFINITY ? 0.f : -q.m;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (cc[h] >= 0)
+                    sm.eqc[cc[h]] = DK == DRAFT_LOGITS ? ex2((dc[h] + negmq) * k) : dc[h];
+            if (lane == 0) {
+                sm.mq[nd] = q.m;
+                sm.sq[nd] = q.s;
+                sm.dflags[nd] = q.flags;
+            }
+        }
+    }
+    __syncthreads();
 }
 
 template <int DT, int DK, int DDT>
@@ -515,7 +599,8 @@ __device__ __forceinline__ Ctx node_ctx(const SampleWalkParams &P, const Smem &s
 }
 
 // Point drafts fit 64 registers (2 CTAs per SM); dense drafts keep more live values.
-template <int DT, int DK, int DDT>
+// LAZY: no row-statistics kernel ran; the walk streams only the rows it visits.
+template <int DT, int DK, int DDT, bool LAZY>
 __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     walk_sample_kernel(SampleWalkParams P) {
     __shared__ Smem sm;
@@ -526,7 +611,11 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     const int N = P.N;
     const size_t base = (size_t)b * N;
 
-    if (tid < N) {
+    if (tid < N && LAZY) {
+        sm.par[tid] = P.parent[base + tid];
+        sm.tok[tid] = P.tok[base + tid];
+    }
+    if (tid < N && !LAZY) {
         sm.par[tid] = P.parent[base + tid];
         sm.tok[tid] = P.tok[base + tid];
         sm.flags[tid] = P.flags[base + tid];
@@ -561,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     w.await = CMD_NONE;
     w.entering = true;
     w.just_summed = false;
+    w.stats_ready = false;
     if (warp == 0) {
         // Request checks in the oracle's order: parents, draft tokens, uniforms.
         bool bp = false, bt = false, bu = false;
@@ -584,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     int cmd = CMD_NONE;
     for (;;) {
         if (warp == 0) {
-            cmd = advance<DK>(w, sm, N);
+            cmd = advance<DK, LAZY>(w, sm, N);
             if (lane == 0) {
                 sm.cmd = cmd;
                 sm.node = w.node;
@@ -595,6 +685,10 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         __syncthreads();
         cmd = sm.cmd;
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
+        if (LAZY && cmd == CMD_STATS) {
+            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node);
+            continue;
+        }
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
         residual_pass<DT, DK, DDT>(c, sm, subsum);
     }
@@ -655,31 +749,13 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
-    const size_t smem = walk_sample_smem(p.V);
-    walk_sample_kernel<DT, DK, DDT><<<p.B, kThreads, smem, st>>>(p);
+    const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);
+    if (p.lazy)
+        walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
+    else
+        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
-
-size_t walk_sample_smem(int64_t V) { return sizeof(float) * (size_t)((V + kSub - 1) / kSub); }
-
-cudaError_t launch_walk_sample(const SampleWalkParams &p, cudaStream_t st) {
-    if (p.B <= 0) return cudaSuccess;
-    if (p.draft_kind == DRAFT_POINT) {
-        if (p.dtype == 1) return launch_ws<1, DRAFT_POINT, 0>(p, st);
-        return launch_ws<0, DRAFT_POINT, 0>(p, st);
-    }
-    if (p.draft_kind == DRAFT_PROBS_F32) {
-        if (p.dtype == 1) return launch_ws<1, DRAFT_PROBS_F32, 0>(p, st);
-        return launch_ws<0, DRAFT_PROBS_F32, 0>(p, st);
-    }
-    if (p.dtype == 1) {
-        if (p.draft_dtype == 1) return launch_ws<1, DRAFT_LOGITS, 1>(p, st);
-        return launch_ws<1, DRAFT_LOGITS, 0>(p, st);
-    }
-    if (p.draft_dtype == 1) return launch_ws<0, DRAFT_LOGITS, 1>(p, st);
-    return launch_ws<0, DRAFT_LOGITS, 0>(p, st);
-}
-
 }  // namespace specv

@@ -59,18 +59,34 @@ def assert_exact(gpu, ref, rows=None):
 
 
 def compare_sample(gpu, ref, rows=None, max_excluded_frac=0.10):
-    """Identity outside the margins; returns the number of excluded requests."""
-    excl = (ref["decision_margin"] < MARGIN) | (ref["cdf_margin"] < MARGIN)
+    """Identity outside the margins. A request whose decision margin is below 1e-6 is
+    excluded; one whose bonus draw lies within 1e-6 of a CDF boundary must still match in
+    every output except the bonus, and its bonus must be the oracle's or the token across
+    that boundary (cdf_alt). Returns (excluded, near-boundary) counts."""
+    g = {k: (gpu[k][rows] if rows is not None else gpu[k]) for k in KEYS}
+    excl = ref["decision_margin"] < MARGIN
+    near = (ref["cdf_margin"] < MARGIN) & ~excl
     keep = ~excl
+    L = g["accept_len"]
     for k in KEYS:
-        a, b = gpu[k], ref[k]
-        if rows is not None:
-            a = a[rows]
-        a, b = a[keep], b[keep]
+        a, b = g[k].copy(), ref[k].copy()
+        if k == "bonus":
+            a, b = a[keep & ~near], b[keep & ~near]
+        elif k == "out_tokens":
+            idx = np.nonzero(near)[0]
+            a[idx, L[idx]] = b[idx, L[idx]]        # the bonus slot, checked below
+            a, b = a[keep], b[keep]
+        else:
+            a, b = a[keep], b[keep]
         if not np.array_equal(a, b):
             bad = np.argwhere(np.asarray(a != b).reshape(len(a), -1).any(1)).ravel()[:5]
             raise AssertionError(f"{k} differs at kept requests {bad.tolist()}: gpu "
                                  f"{a[bad].tolist()} oracle {b[bad].tolist()}")
+    for i in np.nonzero(near)[0]:
+        gb = int(g["bonus"][i])
+        assert gb in (int(ref["bonus"][i]), int(ref["cdf_alt"][i])), \
+            (i, gb, int(ref["bonus"][i]), int(ref["cdf_alt"][i]))
+        assert g["out_tokens"][i, L[i]] == gb
     n = int(excl.sum())
-    assert n <= max(1, max_excluded_frac * len(excl)), f"{n} margin cases of {len(excl)}"
-    return n
+    assert n <= max(1, max_excluded_frac * len(excl)), f"{n} decision-margin cases of {len(excl)}"
+    return n, int(near.sum())

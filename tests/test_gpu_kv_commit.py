@@ -1,0 +1,104 @@
+"""spec_kv_commit against the KV-commit oracle through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kv_commit as K
+from speculative_decoding_tree_mask_gb300 import binding as G
+from speculative_decoding_tree_mask_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def h():
+    G.load()
+    with G.Handle(64, 64, 1 << 16, 0) as handle:
+        yield handle
+
+
+def _paths(rng, parent):
+    """A random root path per request: (kv_commit, accept_len) as a verify call returns them."""
+    B, N = parent.shape
+    kv = np.full((B, N), -1, np.int32)
+    al = np.zeros(B, np.int32)
+    for b in range(B):
+        node, path = 0, [0]
+        while True:
+            kids = [c for c in range(N) if c and parent[b, c] == node]
+            if not kids or rng.random() < 0.25:
+                break
+            node = int(rng.choice(kids))
+            path.append(node)
+        kv[b, :len(path)] = path
+        al[b] = len(path) - 1
+    return kv, al
+
+
+@pytest.mark.parametrize("src", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("cache", [K.SAME, K.FP8_E4M3, K.FP8_E5M2])
+@pytest.mark.parametrize("layout", [K.NHD, K.HND])
+@pytest.mark.parametrize("D", [128, 36])
+def test_kv_commit_matches_oracle(h, src, cache, layout, D):
+    rng = np.random.default_rng(hash((src, cache, layout, D)) % 2**32)
+    B, N, H, bs = 12, 16, 4, 16
+    parent = np.stack([W.random_trie(rng, N, 6, 3) for _ in range(B)])
+    kv, al = _paths(rng, parent)
+    for b in (5, 7):                                # paths of at least 3 slots
+        node, path = 0, [0]
+        while len(path) < 3:
+            kids = [c for c in range(N) if c and parent[b, c] == node]
+            if not kids:
+                break
+            node = kids[0]
+            path.append(node)
+        kv[b] = -1
+        kv[b, :len(path)] = path
+        al[b] = len(path) - 1
+        assert al[b] >= 2
+    kv[3] = -1                                      # a failed request: nothing is written
+    al[3] = 0
+    max_blocks = 4
+    num_blocks = B * max_blocks + 3
+    table = rng.permutation(num_blocks)[:B * max_blocks].reshape(B, max_blocks).astype(np.int32)
+    pos = rng.integers(0, max_blocks * bs - N, B).astype(np.int32)
+    pos[5] = max_blocks * bs - 1                    # slots past the table: status 5
+    table[7, 1] = num_blocks + 5                    # a block id outside the cache
+    pos[7] = bs - 2
+    kvals = (rng.standard_normal((B, N, H, D)) * 3).astype(np.float32)
+    vvals = (rng.standard_normal((B, N, H, D)) * 3).astype(np.float32)
+    tk = torch.from_numpy(kvals).to(TDT[src])
+    tv = torch.from_numpy(vvals).to(TDT[src])
+    kf, vf = tk.float().numpy(), tv.float().numpy()   # exact values of the source type
+    shape = (num_blocks, bs, H, D) if layout == K.NHD else (num_blocks, H, bs, D)
+    ks, vs = 0.5, 2.0
+    if cache == K.SAME:
+        ck0 = torch.full(shape, -1024.0, dtype=TDT[src])
+        cv0 = ck0.clone()
+        ref_k, ref_v, ref_st = K.kv_commit(kf, vf, kv, al, ck0.float().numpy(),
+                                           cv0.float().numpy(), layout, bs, table, pos)
+    else:
+        ck0 = torch.full(shape, 0x55, dtype=torch.uint8)
+        cv0 = ck0.clone()
+        ref_k, ref_v, ref_st = K.kv_commit(kf, vf, kv, al, ck0.numpy(), cv0.numpy(), layout, bs,
+                                           table, pos, cache_kind=cache, k_scale=ks, v_scale=vs)
+    gk, gv = ck0.to(DEV), cv0.to(DEV)
+    st = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    scale_k = torch.tensor([ks], device=DEV)
+    scale_v = torch.tensor([vs], device=DEV)
+    G.spec_kv_commit(h, tk.to(DEV), tv.to(DEV), torch.from_numpy(kv).to(DEV),
+                     torch.from_numpy(al).to(DEV), gk, gv, layout,
+                     torch.from_numpy(table).to(DEV), torch.from_numpy(pos).to(DEV),
+                     cache_kind=cache, k_scale=scale_k if cache else None,
+                     v_scale=scale_v if cache else None, commit_status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().numpy().tolist() == ref_st.tolist()
+    assert ref_st[5] == K.BAD_SLOT and ref_st[7] == K.BAD_SLOT
+    if cache == K.SAME:
+        assert np.array_equal(gk.cpu().float().numpy(), ref_k)
+        assert np.array_equal(gv.cpu().float().numpy(), ref_v)
+    else:
+        assert np.array_equal(gk.cpu().numpy(), ref_k)
+        assert np.array_equal(gv.cpu().numpy(), ref_v)

@@ -249,3 +249,17 @@ def test_two_token_closed_form(orc, T):
             assert res["accept_len"][0] == want
             if want == 0:
                 assert res["bonus"][0] == 1     # token 0 removed from the residual
+
+
+def test_cdf_alt_is_the_token_across_the_nearer_boundary(orc):
+    """Root only, V = 4 equal logits: p = 1/4 each, boundaries at 1/4, 1/2, 3/4."""
+    logits = np.zeros((3, 1, 4), np.float32)
+    tok = np.zeros((3, 1), np.int32)
+    par = np.full((3, 1), -1, np.int32)
+    u = np.array([[0.0, np.float32(0.5) + np.float32(6e-8)],      # just above 1/2: token 2, alt 1
+                  [0.0, np.float32(0.75) - np.float32(6e-8)],     # just below 3/4: token 2, alt 3
+                  [0.0, 0.6]], np.float32)                        # mid-interval: alt 2 only if
+    r = orc.verify_sample(logits, tok, par, 1.0, u)               # it is the nearer side
+    assert r["bonus"].tolist() == [2, 2, 2]
+    assert r["cdf_alt"][:2].tolist() == [1, 3]
+    assert (r["cdf_margin"][:2] < 1e-6).all() and r["cdf_margin"][2] > 1e-2

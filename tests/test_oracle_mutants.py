@@ -34,8 +34,8 @@ MUTANTS = {
     "dense_accept_against_p": ("if (lhs < r[x]) {", "if (lhs < p[x]) {"),
     "temperature_dropped": ("p[v] = exp((elem(row, dtype, v) - m) / T);",
                             "p[v] = exp((elem(row, dtype, v) - m));"),
-    "bonus_uniform_slot": ("inv_cdf(r, V, (double)u[N], &cm);\n    *cmargin = cm;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row",
-                           "inv_cdf(r, V, (double)u[N - 1], &cm);\n    *cmargin = cm;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row"),
+    "bonus_uniform_slot": ("inv_cdf(r, V, (double)u[N], &cm, &alt);\n    *cmargin = cm;\n    *calt = (int32_t)alt;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row",
+                           "inv_cdf(r, V, (double)u[N - 1], &cm, &alt);\n    *cmargin = cm;\n    *calt = (int32_t)alt;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row"),
     "draft_row_of_child": ("draft_row(draft, draft_kind, draft_dtype, grow, V, T, q)",
                            "draft_row(draft, draft_kind, draft_dtype, grow + 1, V, T, q)"),
     "greedy_ignores_token": ("if (par[c] == node && tok[c] == a) {", "if (par[c] == node) {"),
