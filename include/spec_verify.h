@@ -162,6 +162,10 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
  * differ from it only where float32 rounding of a sum decides (the same margin cases as
  * against the float64 reference). Rows are streamed one after another along the path, so the
  * latency grows with the accepted length.
+ * Here (only) logits and draft may also be page-locked host memory that the device maps at
+ * the same address (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped on a
+ * system with unified addressing): the visited rows are then read directly over the host
+ * link, with no copy of the other rows. Other host memory returns SPEC_ERR_ARG.
  */
 int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
                             int64_t V, const int32_t *draft_token, const int32_t *parent,

@@ -87,6 +87,18 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _ptr_dev_or_pinned(t):
+    """Logits of the lazy calls: a CUDA tensor, or a page-locked host tensor (the library
+    checks that the device maps it at the same address)."""
+    if t is None:
+        return None
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("logits must be a CUDA tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -187,10 +199,10 @@ def spec_verify_greedy_lazy(h: Handle, logits, draft_token, parent, accept_len, 
     """Greedy verification reading only the rows on the accepted path."""
     B, N, V = logits.shape
     _check(load().spec_verify_greedy_lazy(
-        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
+        h.ptr, _ptr_dev_or_pinned(logits), _dtype_code(logits), B, N, V,
         _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
         _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
-        _stream(stream, logits.device)), "spec_verify_greedy_lazy")
+        _stream(stream, draft_token.device)), "spec_verify_greedy_lazy")
 
 
 def spec_verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature: float, uniforms,
@@ -204,11 +216,11 @@ def spec_verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature:
     if draft is not None and draft_kind == SPEC_DRAFT_PROBS_F32 and draft.dtype != torch.float32:
         raise TypeError("draft probabilities must be float32")
     _check(load().spec_verify_sample_lazy(
-        h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
-        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")), _ptr(draft),
-        int(draft_kind), ddt, float(temperature), _ptr(uniforms), _ptr(accept_len),
-        _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
-        _stream(stream, logits.device)), "spec_verify_sample_lazy")
+        h.ptr, _ptr_dev_or_pinned(logits), _dtype_code(logits), B, N, V,
+        _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
+        _ptr_dev_or_pinned(draft), int(draft_kind), ddt, float(temperature), _ptr(uniforms),
+        _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus), _ptr(status),
+        _stream(stream, draft_token.device)), "spec_verify_sample_lazy")
 
 
 def spec_row_stats(h: Handle, logits, N: int, temperature: float, row_max, row_sum, row_argmax,
@@ -291,7 +303,7 @@ def verify_sample(h: Handle, logits, draft_token, parent, temperature, uniforms,
 def verify_greedy_lazy(h: Handle, logits, draft_token, parent, out: dict | None = None,
                        stream=None) -> dict:
     B, N, _ = logits.shape
-    out = out or alloc_outputs(B, N, logits.device)
+    out = out or alloc_outputs(B, N, draft_token.device)
     spec_verify_greedy_lazy(h, logits, draft_token, parent, out["accept_len"], out["out_tokens"],
                             out["kv_commit"], out["bonus"], out["status"], stream)
     return out
@@ -300,7 +312,7 @@ def verify_greedy_lazy(h: Handle, logits, draft_token, parent, out: dict | None 
 def verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature, uniforms, draft=None,
                        draft_kind=SPEC_DRAFT_POINT, out: dict | None = None, stream=None) -> dict:
     B, N, _ = logits.shape
-    out = out or alloc_outputs(B, N, logits.device)
+    out = out or alloc_outputs(B, N, draft_token.device)
     spec_verify_sample_lazy(h, logits, draft_token, parent, temperature, uniforms,
                             out["accept_len"], out["out_tokens"], out["kv_commit"], out["bonus"],
                             out["status"], draft, draft_kind, stream)

@@ -72,6 +72,19 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
 
+// Lazy calls read logits where they live: device memory, or page-locked host memory that
+// the device reaches at the same address (read over the host link). Anything else (pageable
+// host memory, a registration mapped at another address) is refused.
+bool readable_by_device(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 int check_common(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
                  const int32_t *tok, const int32_t *parent, const int32_t *accept_len,
                  const int32_t *out_tokens, const int32_t *kv_commit, const int32_t *bonus,
@@ -331,6 +344,7 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
     if (rc != SPEC_OK || B == 0) return rc;
     DeviceScope ds(h->device);
     if (!ds.ok()) return SPEC_ERR_CUDA;
+    if (!readable_by_device(logits)) return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     LazyGreedyParams lp;
     lp.B = B;
@@ -372,6 +386,7 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
     }
     DeviceScope ds(h->device);
     if (!ds.ok()) return SPEC_ERR_CUDA;
+    if (!readable_by_device(logits) || (draft && !readable_by_device(draft))) return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     SampleWalkParams wp{};
     wp.B = B;

@@ -201,3 +201,36 @@ def test_lazy_profiling_classes(h):
     prof = G.spec_profile_end(h)
     assert prof["lazy_sample"][1] == 1 and prof["lazy_greedy"][1] == 1
     assert prof["row_stats"][1] == 0
+
+
+def test_lazy_reads_pinned_host_logits(h, orc):
+    w = W.WORKLOADS["sampling_trie"].scaled(B=16, V=20000, boost=12.0, seed=21)
+    x = W.make(w, device=DEV)
+    host = x["logits"].cpu().pin_memory()
+    a = lazy_sample(h, host, x["draft_token"], x["parent"], 0.7, x["uniforms"])
+    b = lazy_sample(h, x["logits"], x["draft_token"], x["parent"], 0.7, x["uniforms"])
+    for k in PY.KEYS:
+        assert np.array_equal(a[k], b[k]), k
+    g1 = lazy_greedy(h, host, x["draft_token"], x["parent"])
+    g2 = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
+    for k in PY.KEYS:
+        assert np.array_equal(g1[k], g2[k]), k
+
+
+def test_lazy_refuses_pageable_host_logits(h):
+    """A pageable host pointer is rejected by the library before any launch."""
+    import ctypes
+    w = W.WORKLOADS["sampling_trie"].scaled(B=2, N=4, V=64, seed=22)
+    x = W.make(w, device=DEV)
+    pageable = np.zeros((2, 4, 64), np.uint16)
+    out = G.alloc_outputs(2, 4, DEV)
+    lib = G.load()
+    rc = lib.spec_verify_greedy_lazy(
+        h.ptr, ctypes.c_void_p(pageable.ctypes.data), G.SPEC_BF16, 2, 4, 64,
+        ctypes.c_void_p(x["draft_token"].data_ptr()), ctypes.c_void_p(x["parent"].data_ptr()),
+        ctypes.c_void_p(out["accept_len"].data_ptr()),
+        ctypes.c_void_p(out["out_tokens"].data_ptr()),
+        ctypes.c_void_p(out["kv_commit"].data_ptr()), ctypes.c_void_p(out["bonus"].data_ptr()),
+        ctypes.c_void_p(out["status"].data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == G.SPEC_ERR_ARG
