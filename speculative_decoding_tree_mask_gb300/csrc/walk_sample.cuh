@@ -52,6 +52,7 @@ struct Smem {
     float u[kMaxN + 1];
     int path[kMaxN];
     int R[kMaxN];        // rejected tokens at the current node, ascending
+    float RE[kMaxN];     // e_t of each rejected token (same order as R)
     float invZ[kMaxN];   // dense: 1 / Z of each normalised residual level (0: level kept)
     double zinv[kMaxN];  // dense: 1 / Z of each level in float64 (0: level kept)
     int nR, nlev, pending;
@@ -59,6 +60,8 @@ struct Smem {
     double total;
     double wtot[kWarps];
     int haskids;                       // lazy statistics: the node has children
+    int subsum_node;                   // node whose rescaled sub-tile sums are in subsum[]
+    int wflag[kWarps];
     rowpass::Part part[kWarps], part_out;
 };
 
@@ -465,12 +468,21 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
                 if (!dup) {
                     const int pos = __popc(__ballot_sync(full, r0 < t)) +
                                     __popc(__ballot_sync(full, r1 < t));
+                    const float e0v = lane < nR ? sm.RE[lane] : 0.f;
+                    const float e1v = lane + 32 < nR ? sm.RE[lane + 32] : 0.f;
                     __syncwarp();
-                    if (lane < nR && lane >= pos) sm.R[lane + 1] = r0;
-                    if (lane + 32 < nR && lane + 32 >= pos) sm.R[lane + 33] = r1;
+                    if (lane < nR && lane >= pos) {
+                        sm.R[lane + 1] = r0;
+                        sm.RE[lane + 1] = e0v;
+                    }
+                    if (lane + 32 < nR && lane + 32 >= pos) {
+                        sm.R[lane + 33] = r1;
+                        sm.RE[lane + 33] = e1v;
+                    }
                     __syncwarp();
                     if (lane == 0) {
                         sm.R[pos] = t;
+                        sm.RE[pos] = sm.ec[c];
                         sm.nR = nR + 1;
                     }
                     __syncwarp();
@@ -506,11 +518,101 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
     }
 }
 
+// Lazy walks, target row: one pass over 256-element sub-tiles (the bonus search's tiling)
+// gives every sub-tile's max M_j and S_j = sum 2^((z - M_j) k); the row's M = max M_j and
+// S = sum S_j 2^((M_j - M) k), and subsum[j] keeps S_j rescaled to M, so a bonus drawn from
+// this row re-reads one sub-tile instead of the whole row. Results land in sm.part_out
+// (m, s, flags). All threads call it; it ends synchronised.
+template <int DT>
+__device__ void lazy_row_pass(const char *row, int V, float k, Smem &sm, float *subsum,
+                              float *submax) {
+    constexpr int U = DT == 1 ? 4 : 2;   // sub-tiles in flight per warp
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nsub = (V + kSub - 1) / kSub;
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const int nfull = vec ? V / kSub : 0;
+    bool nan = false;
+
+    auto tile = [&](int j, const float (&x)[8]) {
+        float lm = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            nan |= x[q] != x[q];
+            lm = fmaxf(lm, x[q]);
+        }
+        float wm = lm;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(full, wm, o));
+        float sj = 0.f;
+        if (wm != -INFINITY && wm != INFINITY) {
+            const float negm = -wm;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sj += ex2((x[q] + negm) * k);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sj += __shfl_xor_sync(full, sj, o);
+        if (lane == 0) {
+            subsum[j] = sj;
+            submax[j] = wm;
+        }
+    };
+
+    for (int j0 = warp; j0 < nfull; j0 += kWarps * U) {
+        uint4 za[U], zb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kWarps;
+            if (j < nfull) fetch<DT>(row, j * kSub + lane * 8, za[u], zb[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * kWarps;
+            if (j < nfull) {
+                float x[8];
+                shifted8<DT>(za[u], zb[u], 0.f, x);
+                tile(j, x);
+            }
+        }
+    }
+    for (int j = nfull + warp; j < nsub; j += kWarps) {
+        float x[8];
+        shifted8_scalar<DT>(row, j * kSub + lane * 8, V, 0.f, -INFINITY, x);
+        tile(j, x);
+    }
+    const bool wnan = __any_sync(full, nan);
+    if (lane == 0) sm.wflag[warp] = wnan;
+    __syncthreads();
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int j = lane; j < nsub; j += 32) M = fmaxf(M, submax[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(full, M, o));
+        KSum acc;
+        for (int j = lane; j < nsub; j += 32) {
+            const float mj = submax[j];
+            const float r = (mj == -INFINITY || M == INFINITY) ? 0.f : subsum[j] * ex2((mj - M) * k);
+            subsum[j] = r;
+            acc.add(r);
+        }
+        double S = acc.value();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(full, S, o);
+        int flags = (lane < kWarps && sm.wflag[lane]) ? rowpass::F_NAN : 0;
+        flags = __reduce_or_sync(full, flags);
+        if (M == INFINITY) flags |= rowpass::F_POSINF;
+        if (M == -INFINITY) flags |= rowpass::F_ALLNEG;
+        if (lane == 0) sm.part_out = rowpass::Part{M, (float)S, 0, flags};
+    }
+    __syncthreads();
+}
+
 // Lazy walks: the statistics of the node's target row (and, for dense drafts of an inner
 // node, of its draft row) with the same per-element arithmetic as the row-statistics
 // kernel, plus e_t at the children's tokens. All threads call it; it ends synchronised.
 template <int DT, int DK, int DDT>
-__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd) {
+__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd,
+                           float *subsum, float *submax) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
     constexpr int kDEsz = kDDT == 1 ? 2 : 4;
@@ -535,8 +637,9 @@ __device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int
         const bool kids = __any_sync(0xffffffffu, any);
         if (lane == 0) sm.haskids = kids;
     }
-    const rowpass::Part p =
-        rowpass::cta_row_stats<DT, ROW_SAMPLE, kThreads, 4>(zrow, V, k, sm.part, &sm.part_out);
+    lazy_row_pass<DT>(zrow, (int)V, k, sm, subsum, submax);
+    const rowpass::Part p = sm.part_out;
+    if (threadIdx.x == 0) sm.subsum_node = nd;
     if (warp == 0) {
         const float negm = p.m == -INFINITY ? 0.f : -p.m;
 #pragma unroll
@@ -604,7 +707,8 @@ template <int DT, int DK, int DDT, bool LAZY>
 __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     walk_sample_kernel(SampleWalkParams P) {
     __shared__ Smem sm;
-    extern __shared__ float subsum[];
+    extern __shared__ float subsum[];   // sub-tile sums; lazy walks add the sub-tile maxima
+    float *submax = subsum + (P.V + kSub - 1) / kSub;
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
@@ -637,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         sm.nlev = 0;
         sm.pending = 0;
         sm.bonus = -1;
+        sm.subsum_node = -1;
     }
     __syncthreads();
 
@@ -686,16 +791,34 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         cmd = sm.cmd;
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
         if (LAZY && cmd == CMD_STATS) {
-            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node);
+            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node, subsum, submax);
             continue;
         }
+        if (tid == 0) sm.subsum_node = -1;   // the pass overwrites the stored sums
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
         residual_pass<DT, DK, DDT>(c, sm, subsum);
     }
 
     if (cmd == CMD_BONUS) {
         const float ub = sm.u[N];
-        for (int attempt = 0; attempt < 3; ++attempt) {
+        bool drawn = false;
+        if (LAZY && DK == DRAFT_POINT && sm.subsum_node == sm.node) {
+            // Single pass: the stored sub-tile sums of this row minus the rejected tokens.
+            if (tid == 0)
+                for (int i = 0; i < sm.nR; ++i) {
+                    const int j = sm.R[i] / kSub;
+                    subsum[j] = fmaxf(subsum[j] - sm.RE[i], 0.f);
+                }
+            __syncthreads();
+            const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
+            if (warp == 0) {
+                const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub);
+                if (lane == 0) sm.bonus = v;
+            }
+            __syncthreads();
+            drawn = sm.bonus >= 0;
+        }
+        for (int attempt = 0; attempt < 3 && !drawn; ++attempt) {
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
             residual_pass<DT, DK, DDT>(c, sm, subsum);
             if (warp == 0) {
@@ -749,11 +872,19 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
-    const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);
-    if (p.lazy)
+    const size_t nsub = (size_t)((p.V + kSub - 1) / kSub);
+    if (p.lazy) {
+        const size_t smem = 2 * sizeof(float) * nsub;   // sub-tile sums and maxima
+        if (smem > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(walk_sample_kernel<DT, DK, DDT, true>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)smem);
+            if (e != cudaSuccess) return e;
+        }
         walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
-    else
-        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, smem, st>>>(p);
+    } else {
+        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, sizeof(float) * nsub, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
