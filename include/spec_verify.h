@@ -69,11 +69,14 @@ enum {
     SPEC_REQ_BAD_ROW = 3,       /* a row the walk needs holds NaN / +inf or is all -inf
                                    (for probabilities: NaN, inf or a negative entry) */
     SPEC_REQ_BAD_UNIFORM = 4,   /* a uniform in slots 1..N is NaN or outside [0, 1) */
-    SPEC_REQ_BAD_SLOT = 5       /* KV commit: a slot maps outside the block table or cache */
+    SPEC_REQ_BAD_SLOT = 5,      /* KV commit: a slot maps outside the block table or cache */
+    SPEC_REQ_BAD_BUDGET = 6     /* the request's node budget (spec_set_node_budget) is
+                                   outside [1, N] */
 };
 
 enum { SPEC_KV_NHD = 0, SPEC_KV_HND = 1 };  /* paged KV cache layouts */
 enum { SPEC_CACHE_SAME = 0, SPEC_CACHE_FP8_E4M3 = 1, SPEC_CACHE_FP8_E5M2 = 2 };
+enum { SPEC_SCALE_TENSOR = 0, SPEC_SCALE_PER_TOKEN = 1 };   /* fp8 KV scale forms */
 
 /* Row-statistics flag bits (spec_row_stats row_flags). */
 enum { SPEC_ROW_NAN = 1, SPEC_ROW_POSINF = 2, SPEC_ROW_ALL_NEGINF = 4 };
@@ -88,7 +91,8 @@ enum {
     SPEC_K_LAZY_GREEDY = 5,
     SPEC_K_LAZY_SAMPLE = 6,
     SPEC_K_KV_COMMIT = 7,
-    SPEC_K_COUNT = 8
+    SPEC_K_BUDGET = 8,          /* adaptive node-budget update */
+    SPEC_K_COUNT = 9
 };
 
 /*
@@ -190,8 +194,11 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
  *                   (SPEC_CACHE_SAME) or one byte of fp8 (SPEC_CACHE_FP8_E4M3 / _E5M2);
  *   block_table     int32 [B, max_blocks]: cache block of each block_size tokens of request b;
  *   seq_pos         int32 [B]: sequence position of slot 0 (the root);
- *   k_scale, v_scale        device float scalars for fp8 caches (NULL = 1): the cache stores
+ *   k_scale, v_scale        device float32 scales for fp8 caches (NULL = 1): the cache stores
  *                   the fp8 rounding (nearest, ties to even, saturated) of x / scale;
+ *   scale_per_token SPEC_SCALE_TENSOR: each scale is one value; SPEC_SCALE_PER_TOKEN: each is
+ *                   float32 [B, N], the scale of source token (b, node) (the commit kernel of
+ *                   IluvatarLabs/vllm PR #3 takes scalar and per-token scales);
  *   commit_status   int32 [B] (may be NULL): SPEC_REQ_BAD_SLOT if a slot's position or block
  *                   falls outside the table or the cache (that slot is skipped), else 0.
  * Slot j of request b (j = 0..accept_len[b]) is written at position seq_pos[b] + j. Requests
@@ -202,7 +209,7 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
                    void *cache_k, void *cache_v, int cache_kind, int layout, int block_size,
                    int64_t num_blocks, const int32_t *block_table, int max_blocks,
                    const int32_t *seq_pos, const float *k_scale, const float *v_scale,
-                   int32_t *commit_status, void *stream);
+                   int scale_per_token, int32_t *commit_status, void *stream);
 
 /*
  * The vocabulary-streaming row statistics on their own (the first stage of both verify
@@ -229,6 +236,61 @@ int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N
  */
 int spec_profile_begin(spec_handle h);
 int spec_profile_end(spec_handle h, float *ms_per_class, int32_t *launches_per_class);
+
+/*
+ * Node budget (IluvatarLabs/vllm PR #3, adaptive mode: the number of speculative tokens
+ * verified per step follows the recent acceptance ratio, and the mask computation is replayed
+ * from captured CUDA graphs). Draft nodes are in topological order, so the first n nodes of a
+ * tree always form a tree themselves; a budget of n keeps exactly those.
+ *
+ * spec_set_node_budget makes every later verify call on the handle (eager and lazy, greedy
+ * and sampling) read n_active[b] -- a DEVICE int32 [>= B] array owned by the caller, read by
+ * the kernels when they run -- and verify request b as the tree of its nodes 0..n-1 with
+ * n = n_active[b]: nodes >= n do not exist for that call (their rows are not read, their
+ * tokens, parents and uniform slots are not checked), while shapes, the bonus uniform slot N
+ * and the [B, N] output layout stay as they are. A value outside [1, N] gives that request
+ * SPEC_REQ_BAD_BUDGET. Because the value is read on the device, a CUDA graph captured once
+ * follows every new budget on replay. NULL (the default) verifies all N nodes. The array must
+ * stay valid while it is set. spec_row_stats and spec_verify_greedy_noalloc ignore it.
+ */
+int spec_set_node_budget(spec_handle h, const int32_t *n_active);
+
+/*
+ * Budget controller, one update per verify step, entirely on the device (no host
+ * synchronisation, so it can sit inside a captured graph next to the verify call).
+ *   params (host struct, copied at the call):
+ *     target   acceptance ratio to hold, in (0, 1];
+ *     alpha    weight of the newest step in the moving average, in (0, 1];
+ *     band     dead band around the target, finite and >= 0;
+ *     n_min, n_max   budget limits, 1 <= n_min <= n_max <= N;  step   change per update, >= 1.
+ *   accept_len, status  int32 [B]: outputs of the verify call the budget governed;
+ *   parent      int32 [B, N]: that call's trees;
+ *   state       DEVICE spec_budget_state, caller-owned and initialised by the caller (ema,
+ *               budget; steps = 0), read and rewritten by the update;
+ *   n_active    DEVICE int32 [B]: on entry the budgets the verify call used; on exit every
+ *               entry holds the new budget.
+ * Update: over requests with status 0 and a budget n in [1, N], A = sum of accept_len and
+ * D = sum of the deepest node depth among nodes 0..n-1 (the most that request could have
+ * accepted). If D > 0: ratio = A / D, ema <- (1 - alpha) * ema + alpha * ratio, steps += 1;
+ * the budget (first clamped to [n_min, n_max]) rises by step (at most n_max) when
+ * ema > target + band and falls by step (at least n_min) when ema < target - band. If D == 0
+ * the average is unchanged. All of it is evaluated in float64 in this order, so the result is
+ * reproducible exactly. Bad parameters return SPEC_ERR_ARG and launch nothing.
+ */
+typedef struct {
+    double target, alpha, band;
+    int32_t n_min, n_max, step;
+} spec_budget_params;
+
+typedef struct {
+    double ema;       /* moving average of the acceptance ratio */
+    int32_t budget;   /* node budget for the next step */
+    int32_t steps;    /* updates that saw at least one usable request */
+} spec_budget_state;
+
+int spec_budget_update(spec_handle h, const spec_budget_params *params,
+                       const int32_t *accept_len, const int32_t *status, const int32_t *parent,
+                       int B, int N, spec_budget_state *state, int32_t *n_active, void *stream);
 
 /* Static description of a SPEC_ERR_* code. */
 const char *spec_error_string(int code);

@@ -12,7 +12,9 @@ then the accepted nodes in path order) are written at sequence positions seq_pos
     block = block_table[b][p // block_size], offset = p % block_size,
     NHD cache [num_blocks, block_size, H, D], HND cache [num_blocks, H, block_size, D].
 fp8 caches store fp8(x / scale) with x / scale rounded to float32 first, then rounded to the
-nearest fp8 value (ties to the even code) and saturated to the largest finite value.
+nearest fp8 value (ties to the even code) and saturated to the largest finite value. The
+commit kernel takes a scalar scale or one scale per token: a scale given as a [B, N] array is
+the scale of source token (b, node).
 A request whose kv_commit[b][0] < 0 (verification failed) writes nothing; a slot whose block
 lies outside the table or the cache writes nothing and sets commit_status[b] = 5.
 """
@@ -109,7 +111,8 @@ def kv_commit(src_k, src_v, kv_commit_idx, accept_len, cache_k, cache_v, layout,
                 if cache_kind == SAME:
                     val = x
                 else:
-                    q = (x.astype(np.float32) / np.float32(scale)).astype(np.float32)
+                    s = scale[b, node] if np.ndim(scale) == 2 else scale
+                    q = (x.astype(np.float32) / np.float32(s)).astype(np.float32)
                     val = fp8_encode(q, cache_kind).reshape(H, D)
                 if layout == NHD:
                     cache[blk, off] = val

@@ -22,11 +22,22 @@ SPEC_REQ_OK, SPEC_REQ_BAD_PARENT, SPEC_REQ_BAD_TOKEN, SPEC_REQ_BAD_ROW, SPEC_REQ
     0, 1, 2, 3, 4
 SPEC_ROW_NAN, SPEC_ROW_POSINF, SPEC_ROW_ALL_NEGINF = 1, 2, 4
 KERNEL_CLASSES = ("tree_mask", "row_stats", "draft_stats", "walk_greedy", "walk_sample",
-                  "lazy_greedy", "lazy_sample", "kv_commit")
+                  "lazy_greedy", "lazy_sample", "kv_commit", "budget")
 SPEC_F16 = 2
 SPEC_REQ_BAD_SLOT = 5
+SPEC_REQ_BAD_BUDGET = 6
 SPEC_KV_NHD, SPEC_KV_HND = 0, 1
 SPEC_CACHE_SAME, SPEC_CACHE_FP8_E4M3, SPEC_CACHE_FP8_E5M2 = 0, 1, 2
+SPEC_SCALE_TENSOR, SPEC_SCALE_PER_TOKEN = 0, 1
+
+
+
+class BudgetParams(ctypes.Structure):
+    """spec_budget_params: target ratio, moving-average weight, dead band, limits, step."""
+    _fields_ = [("target", ctypes.c_double), ("alpha", ctypes.c_double),
+                ("band", ctypes.c_double), ("n_min", ctypes.c_int32),
+                ("n_max", ctypes.c_int32), ("step", ctypes.c_int32)]
+
 
 _lock = threading.Lock()
 _lib = None
@@ -58,8 +69,11 @@ def load() -> ctypes.CDLL:
             lib.spec_row_stats.argtypes = [P, P, i32, i32, i32, i64, f32, P, P, P, P, P, P, P, P]
             lib.spec_verify_greedy_lazy.argtypes = lib.spec_verify_greedy.argtypes
             lib.spec_kv_commit.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32,
-                                           i32, i32, i64, P, i32, P, P, P, P, P]
+                                           i32, i32, i64, P, i32, P, P, P, i32, P, P]
             lib.spec_verify_sample_lazy.argtypes = lib.spec_verify_sample.argtypes
+            lib.spec_set_node_budget.argtypes = [P, P]
+            lib.spec_budget_update.argtypes = [P, ctypes.POINTER(BudgetParams), P, P, P, i32,
+                                               i32, P, P, P]
             lib.spec_profile_begin.argtypes = [P]
             lib.spec_profile_end.argtypes = [P, P, P]
             lib.spec_error_string.argtypes = [i32]
@@ -245,19 +259,66 @@ def spec_kv_commit(h: Handle, src_k, src_v, kv_commit, accept_len, cache_k, cach
                    block_table, seq_pos, cache_kind: int = SPEC_CACHE_SAME, k_scale=None,
                    v_scale=None, commit_status=None, stream=None):
     """Copy the K/V of the root and the accepted nodes ([B, N, H, D]) into a paged cache
-    (NHD [blocks, block_size, H, D] or HND [blocks, H, block_size, D]); fp8 caches are uint8."""
+    (NHD [blocks, block_size, H, D] or HND [blocks, H, block_size, D]); fp8 caches are uint8.
+    Scales: float32 tensors of one element, or [B, N] (one per source token)."""
     B, N, H, D = src_k.shape
     if layout == SPEC_KV_NHD:
         num_blocks, block_size = cache_k.shape[0], cache_k.shape[1]
     else:
         num_blocks, block_size = cache_k.shape[0], cache_k.shape[2]
+    scale_mode = SPEC_SCALE_TENSOR
+    given = [sc for sc in (k_scale, v_scale) if sc is not None]
+    if any(sc.dtype != torch.float32 for sc in given):
+        raise TypeError("scales must be float32")
+    if any(sc.numel() != 1 for sc in given):
+        if not all(tuple(sc.shape) == (B, N) for sc in given):
+            raise ValueError("scales must all be single values or all [B, N]")
+        scale_mode = SPEC_SCALE_PER_TOKEN
     _check(load().spec_kv_commit(
         h.ptr, _ptr(src_k), _ptr(src_v), _kv_dtype(src_k), B, N, H, D,
         _ptr(_i32(kv_commit, "kv_commit")), _ptr(_i32(accept_len, "accept_len")), _ptr(cache_k),
         _ptr(cache_v), int(cache_kind), int(layout), int(block_size), int(num_blocks),
         _ptr(_i32(block_table, "block_table")), int(block_table.shape[1]),
-        _ptr(_i32(seq_pos, "seq_pos")), _ptr(k_scale), _ptr(v_scale), _ptr(commit_status),
+        _ptr(_i32(seq_pos, "seq_pos")), _ptr(k_scale), _ptr(v_scale), scale_mode,
+        _ptr(commit_status),
         _stream(stream, src_k.device)), "spec_kv_commit")
+
+
+def spec_set_node_budget(h: Handle, n_active):
+    """Later verify calls on ``h`` verify request b as its first n_active[b] nodes (device
+    int32 [>= B], read when the kernels run); None verifies every node."""
+    if n_active is not None:
+        _i32(n_active, "n_active")
+    _check(load().spec_set_node_budget(h.ptr, _ptr(n_active)), "spec_set_node_budget")
+    h.n_active = n_active   # keep the array alive while the handle reads it
+
+
+def spec_budget_update(h: Handle, params: BudgetParams, accept_len, status, parent, state,
+                       n_active, stream=None):
+    """One controller update on the device; ``state`` is a tensor from budget_state()."""
+    B, N = parent.shape
+    if state.dtype != torch.float64 or state.numel() != 2:
+        raise TypeError("state must be the float64 [2] tensor made by budget_state()")
+    _check(load().spec_budget_update(
+        h.ptr, ctypes.byref(params), _ptr(_i32(accept_len, "accept_len")),
+        _ptr(_i32(status, "status")), _ptr(_i32(parent, "parent")), B, N, _ptr(state),
+        _ptr(_i32(n_active, "n_active")), _stream(stream, parent.device)), "spec_budget_update")
+
+
+def budget_state(ema: float, budget: int, device, steps: int = 0) -> torch.Tensor:
+    """A device spec_budget_state {double ema; int32 budget; int32 steps} in a float64 [2]."""
+    t = torch.zeros(2, dtype=torch.float64)
+    t[0] = float(ema)
+    t[1:].view(torch.int32)[0] = int(budget)
+    t[1:].view(torch.int32)[1] = int(steps)
+    return t.to(device)
+
+
+def read_budget_state(state: torch.Tensor):
+    """-> (ema, budget, steps) of a state tensor (synchronises with the device)."""
+    t = state.cpu()
+    iv = t[1:].view(torch.int32)
+    return float(t[0]), int(iv[0]), int(iv[1])
 
 
 def spec_profile_begin(h: Handle):

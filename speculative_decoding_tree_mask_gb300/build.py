@@ -18,7 +18,7 @@ OBJDIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libspecverify.so")
 SOURCES = ["api.cu", "row_stats.cu", "tree_mask.cu", "walk_greedy.cu", "walk_sample_point.cu",
            "walk_sample_dense.cu", "walk_sample_logits_bf16.cu", "walk_sample_logits_f32.cu",
-           "lazy_greedy.cu", "kv_commit.cu", "noalloc.cu"]
+           "lazy_greedy.cu", "kv_commit.cu", "noalloc.cu", "budget.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

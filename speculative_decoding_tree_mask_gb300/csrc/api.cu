@@ -28,6 +28,7 @@ struct spec_ctx {
     float *m = nullptr, *s = nullptr, *pc = nullptr, *mq = nullptr, *sq = nullptr,
           *qc = nullptr;
     int32_t *arg = nullptr, *flags = nullptr, *dflags = nullptr;
+    const int32_t *n_active = nullptr;   // node budget set by spec_set_node_budget
     bool prof = false;
     bool ev_ready = false;
     int nrec = 0;
@@ -128,6 +129,7 @@ int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int6
     rp.s = nullptr;
     rp.arg = h->arg;
     rp.flags = h->flags;
+    rp.n_active = h->n_active;
     int rc = timed(h, SPEC_K_ROW_STATS, st,
                    [&] { return launch_row_stats(rp, dtype, ROW_GREEDY, st); });
     if (rc != SPEC_OK) return rc;
@@ -140,6 +142,7 @@ int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int6
     gp.arg = h->arg;
     gp.flags = h->flags;
     gp.out = out;
+    gp.n_active = h->n_active;
     return timed(h, SPEC_K_WALK_GREEDY, st, [&] { return launch_walk_greedy(gp, st); });
 }
 
@@ -287,6 +290,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     rp.arg = nullptr;
     rp.flags = h->flags;
     rp.pc = h->pc;
+    rp.n_active = h->n_active;
     rc = timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
     if (rc != SPEC_OK) return rc;
 
@@ -332,6 +336,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     wp.qc = h->qc;
     wp.dflags = h->dflags;
     wp.out = out;
+    wp.n_active = h->n_active;
     return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
 }
 
@@ -355,6 +360,7 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
     lp.parent = parent;
     lp.tok = draft_token;
     lp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
+    lp.n_active = h->n_active;
     return timed(h, SPEC_K_LAZY_GREEDY, st, [&] { return launch_lazy_greedy(lp, st); });
 }
 
@@ -403,7 +409,45 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
     wp.draft = draft;
     wp.lazy = 1;
     wp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
+    wp.n_active = h->n_active;
     return timed(h, SPEC_K_LAZY_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
+}
+
+int spec_set_node_budget(spec_handle h, const int32_t *n_active) {
+    if (!h) return SPEC_ERR_ARG;
+    if (n_active && !aligned(n_active, 4)) return SPEC_ERR_ARG;
+    h->n_active = n_active;
+    return SPEC_OK;
+}
+
+int spec_budget_update(spec_handle h, const spec_budget_params *params,
+                       const int32_t *accept_len, const int32_t *status, const int32_t *parent,
+                       int B, int N, spec_budget_state *state, int32_t *n_active, void *stream) {
+    if (!h || !params || !state || !n_active) return SPEC_ERR_ARG;
+    if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
+    const spec_budget_params &q = *params;
+    if (!(q.target > 0.0 && q.target <= 1.0) || !(q.alpha > 0.0 && q.alpha <= 1.0) ||
+        !(q.band >= 0.0) || !std::isfinite(q.band))
+        return SPEC_ERR_ARG;
+    if (q.n_min < 1 || q.n_min > q.n_max || q.n_max > N || q.step < 1) return SPEC_ERR_ARG;
+    if (B > 0 && (!accept_len || !status || !parent)) return SPEC_ERR_ARG;
+    const void *ints[] = {accept_len, status, parent, n_active};
+    for (const void *p : ints)
+        if (p && !aligned(p, 4)) return SPEC_ERR_ARG;
+    if (!aligned(state, alignof(spec_budget_state))) return SPEC_ERR_ARG;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BudgetParams bp;
+    bp.prm = q;
+    bp.accept_len = accept_len;
+    bp.status = status;
+    bp.parent = parent;
+    bp.B = B;
+    bp.N = N;
+    bp.state = state;
+    bp.n_active = n_active;
+    return timed(h, SPEC_K_BUDGET, st, [&] { return launch_budget_update(bp, st); });
 }
 
 int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_dtype, int B,
@@ -411,7 +455,7 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
                    void *cache_k, void *cache_v, int cache_kind, int layout, int block_size,
                    int64_t num_blocks, const int32_t *block_table, int max_blocks,
                    const int32_t *seq_pos, const float *k_scale, const float *v_scale,
-                   int32_t *commit_status, void *stream) {
+                   int scale_per_token, int32_t *commit_status, void *stream) {
     if (!h) return SPEC_ERR_ARG;
     if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
     if (H < 1 || D < 1 || (int64_t)H * D > (int64_t(1) << 24)) return SPEC_ERR_ARG;
@@ -421,6 +465,8 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
         cache_kind != SPEC_CACHE_FP8_E5M2)
         return SPEC_ERR_ARG;
     if (layout != SPEC_KV_NHD && layout != SPEC_KV_HND) return SPEC_ERR_ARG;
+    if (scale_per_token != SPEC_SCALE_TENSOR && scale_per_token != SPEC_SCALE_PER_TOKEN)
+        return SPEC_ERR_ARG;
     if (block_size < 1 || num_blocks < 1 || num_blocks > INT32_MAX || max_blocks < 1)
         return SPEC_ERR_ARG;
     if (B == 0) return SPEC_OK;
@@ -462,6 +508,7 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
     kp.seq_pos = seq_pos;
     kp.k_scale = k_scale;
     kp.v_scale = v_scale;
+    kp.scale_per_token = scale_per_token;
     kp.status = commit_status;
     // 8 elements per thread step: rows of D elements and 16-byte aligned bases.
     const bool vec = D % 8 == 0 && aligned(src_k, 16) && aligned(src_v, 16) &&

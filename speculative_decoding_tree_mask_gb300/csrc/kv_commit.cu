@@ -8,7 +8,8 @@
 // position seq_pos[b] + j:
 //   block = block_table[b][p / block_size], offset = p % block_size,
 //   NHD cache [num_blocks, block_size, H, D], HND cache [num_blocks, H, block_size, D].
-// fp8 caches hold cvt.rn.satfinite(x / scale) (x / scale rounded to float32 first).
+// fp8 caches hold cvt.rn.satfinite(x / scale) (x / scale rounded to float32 first); the scale
+// is one value per tensor or one per source token (b, node).
 // One CTA per (slot, request); CTAs of slots beyond accept_len return at once. Each thread
 // moves 8 elements per step (one or two 16-byte loads, one 16- or 8-byte store).
 
@@ -140,8 +141,9 @@ __global__ void __launch_bounds__(kThreads) kv_commit_kernel(KvCommitParams P) {
     if (blk < 0 || blk >= P.num_blocks) return;
     const int off = p - bi * P.block_size;
     const int H = P.H, D = P.D, HD = H * D;
-    const float ks = P.k_scale ? *P.k_scale : 1.f;
-    const float vs = P.v_scale ? *P.v_scale : 1.f;
+    const size_t si = P.scale_per_token ? (size_t)b * N + node : 0;
+    const float ks = P.k_scale ? P.k_scale[si] : 1.f;
+    const float vs = P.v_scale ? P.v_scale[si] : 1.f;
     const size_t sbase = ((size_t)b * N + node) * (size_t)HD;
     const int step = VEC ? 8 : 1;
     for (int e = threadIdx.x * step; e < HD; e += kThreads * step) {

@@ -32,9 +32,10 @@ __global__ void __launch_bounds__(kThreads, 2) lazy_greedy_kernel(LazyGreedyPara
     const int b = blockIdx.x;
     const int N = P.N;
     const size_t base = (size_t)b * N;
+    const int nb = node_budget(P.n_active, b, N);   // nodes >= nb do not exist in this call
     if (tid < N) {
-        sm.par[tid] = P.parent[base + tid];
-        sm.tok[tid] = P.tok[base + tid];
+        sm.par[tid] = tid < nb ? P.parent[base + tid] : -2;
+        sm.tok[tid] = tid < nb ? P.tok[base + tid] : -1;
     }
     __syncthreads();
     if (warp == 0) {
@@ -42,13 +43,14 @@ __global__ void __launch_bounds__(kThreads, 2) lazy_greedy_kernel(LazyGreedyPara
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = lane + 32 * h;
-            if (i < N) {
+            if (i < nb) {
                 const int p = sm.par[i];
                 bp |= i == 0 ? p != -1 : (p < 0 || p >= i);
                 if (i >= 1) bt |= sm.tok[i] < 0 || sm.tok[i] >= P.V;
             }
         }
-        const int st = __any_sync(full, bp) ? SPEC_REQ_BAD_PARENT
+        const int st = nb == 0 ? SPEC_REQ_BAD_BUDGET
+                       : __any_sync(full, bp) ? SPEC_REQ_BAD_PARENT
                        : __any_sync(full, bt) ? SPEC_REQ_BAD_TOKEN
                                               : SPEC_REQ_OK;
         if (lane == 0) sm.st = st;

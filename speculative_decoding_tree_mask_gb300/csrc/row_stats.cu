@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P
     const bool gather = P.pc != nullptr;
     const int N = P.N;
     const int b = row / N, n = row - b * N;
+    const int nb = node_budget(P.n_active, b, N);   // nodes >= nb do not exist in this call
+    if (n >= nb) return;
     int child[2] = {-1, -1};
     float zc[2] = {0.f, 0.f};
     if (warp == 0 && (gather || P.skip_leaves)) {
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int c = lane + 32 * h;
-            if (c >= 1 && c < N && P.parent[(size_t)b * N + c] == n) {
+            if (c >= 1 && c < nb && P.parent[(size_t)b * N + c] == n) {
                 any = true;
                 const int t = P.tok[(size_t)b * N + c];
                 if (t >= 0 && t < V) {

@@ -11,6 +11,14 @@ namespace specv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kNone = 0x7fffffff;   // "no index yet" in argmax reductions
 
+// Number of nodes request b verifies under a node budget: all N without one, the budget when
+// it lies in [1, N], and 0 (the request is refused) otherwise.
+__device__ __forceinline__ int node_budget(const int32_t *n_active, int b, int N) {
+    if (!n_active) return N;
+    const int n = n_active[b];
+    return n >= 1 && n <= N ? n : 0;
+}
+
 // 2^x on the special-function unit (flushes denormal results to zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;

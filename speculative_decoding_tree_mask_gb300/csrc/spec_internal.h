@@ -29,6 +29,7 @@ struct RowStatsParams {
     int32_t *flags;
     float *pc;               // child_prob output (indexed by child row); may be null
     int pc_normalized;       // 1: pc = e_t / S (probability); 0: pc = e_t (walk input)
+    const int32_t *n_active = nullptr;   // per-request node budget [B]; null = all N rows
 };
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);
@@ -50,6 +51,7 @@ struct GreedyWalkParams {
     const int32_t *parent, *tok;
     const int32_t *arg, *flags;   // row statistics [B, N]
     WalkOutputs out;
+    const int32_t *n_active = nullptr;
 };
 
 cudaError_t launch_walk_greedy(const GreedyWalkParams &p, cudaStream_t st);
@@ -62,6 +64,7 @@ struct LazyGreedyParams {
     const void *logits;
     const int32_t *parent, *tok;
     WalkOutputs out;
+    const int32_t *n_active = nullptr;
 };
 
 cudaError_t launch_lazy_greedy(const LazyGreedyParams &p, cudaStream_t st);
@@ -84,6 +87,7 @@ struct SampleWalkParams {
     const int32_t *dflags;
     int lazy;                     // 1: no row statistics precomputed; stream visited rows only
     WalkOutputs out;
+    const int32_t *n_active = nullptr;
 };
 
 // KV commit of the accepted path into a paged cache (see spec_kv_commit).
@@ -101,10 +105,22 @@ struct KvCommitParams {
     int max_blocks;
     const int32_t *seq_pos;
     const float *k_scale, *v_scale;
+    int scale_per_token;          // 1: scales are [B, N], per source token
     int32_t *status;
 };
 
 cudaError_t launch_kv_commit(const KvCommitParams &p, bool vec, cudaStream_t st);
+
+// Adaptive node-budget update (see spec_budget_update).
+struct BudgetParams {
+    spec_budget_params prm;
+    const int32_t *accept_len, *status, *parent;
+    int B, N;
+    spec_budget_state *state;
+    int32_t *n_active;
+};
+
+cudaError_t launch_budget_update(const BudgetParams &p, cudaStream_t st);
 
 // Dynamic shared memory the sampling walk needs for vocabulary size V.
 size_t walk_sample_smem(int64_t V);

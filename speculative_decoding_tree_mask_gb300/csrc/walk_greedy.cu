@@ -24,13 +24,14 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
     if (b >= P.B) return;
     const int N = P.N;
     const size_t base = (size_t)b * N;
+    const int nb = node_budget(P.n_active, b, N);   // nodes >= nb do not exist in this call
 
     int par[2], tk[2], ag[2], fl[2];
     bool bad_par = false, bad_tok = false;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int i = lane + 32 * h;
-        if (i < N) {
+        if (i < nb) {
             par[h] = P.parent[base + i];
             tk[h] = P.tok[base + i];
             ag[h] = P.arg[base + i];
@@ -44,7 +45,10 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
             fl[h] = 0;
         }
     }
-    int st = __any_sync(full, bad_par) ? 1 : (__any_sync(full, bad_tok) ? 2 : 0);
+    int st = nb == 0                        ? SPEC_REQ_BAD_BUDGET
+             : __any_sync(full, bad_par) ? SPEC_REQ_BAD_PARENT
+             : __any_sync(full, bad_tok) ? SPEC_REQ_BAD_TOKEN
+                                         : SPEC_REQ_OK;
 
     int L = 0, node = 0, a = -1;
     int pth0 = -1, pth1 = -1;   // path[j] lives in lane j % 32, slot j / 32

@@ -714,12 +714,17 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     const int b = blockIdx.x;
     const int N = P.N;
     const size_t base = (size_t)b * N;
+    const int nb = node_budget(P.n_active, b, N);   // nodes >= nb do not exist in this call
 
-    if (tid < N && LAZY) {
+    if (tid < N && tid >= nb) {   // never a child of any node
+        sm.par[tid] = -2;
+        sm.tok[tid] = -1;
+    }
+    if (tid < nb && LAZY) {
         sm.par[tid] = P.parent[base + tid];
         sm.tok[tid] = P.tok[base + tid];
     }
-    if (tid < N && !LAZY) {
+    if (tid < nb && !LAZY) {
         sm.par[tid] = P.parent[base + tid];
         sm.tok[tid] = P.tok[base + tid];
         sm.flags[tid] = P.flags[base + tid];
@@ -762,15 +767,17 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int i = lane + 32 * h;
-            if (i < N) {
+            if (i < nb) {
                 const int p = sm.par[i];
                 bp |= i == 0 ? p != -1 : (p < 0 || p >= i);
                 if (i >= 1) bt |= sm.tok[i] < 0 || sm.tok[i] >= P.V;
             }
+            // uniform slots of the existing children, and the bonus slot N
             const int iu = i + 1;
-            if (iu <= N) bu |= !(sm.u[iu] >= 0.f && sm.u[iu] < 1.f);
+            if (iu < nb || iu == N) bu |= !(sm.u[iu] >= 0.f && sm.u[iu] < 1.f);
         }
-        w.st = __any_sync(full, bp)   ? SPEC_REQ_BAD_PARENT
+        w.st = nb == 0                ? SPEC_REQ_BAD_BUDGET
+               : __any_sync(full, bp) ? SPEC_REQ_BAD_PARENT
                : __any_sync(full, bt) ? SPEC_REQ_BAD_TOKEN
                : __any_sync(full, bu) ? SPEC_REQ_BAD_UNIFORM
                                       : 0;

@@ -56,6 +56,10 @@ def test_host_checks_without_gpu(lib):
     assert lib.spec_verify_sample(None, None, 1, 1, 1, 10, None, None, None, 0, 0, 1.0, None,
                                   None, None, None, None, None, None) == G.SPEC_ERR_ARG
     assert lib.spec_build_tree_mask(None, None, 1, 1, None, None, None, None) == G.SPEC_ERR_ARG
+    assert lib.spec_set_node_budget(None, None) == G.SPEC_ERR_ARG
+    prm = G.BudgetParams(0.5, 0.5, 0.0, 1, 4, 1)
+    assert lib.spec_budget_update(None, ctypes.byref(prm), None, None, None, 1, 4, None, None,
+                                  None) == G.SPEC_ERR_ARG
     assert lib.spec_row_stats(None, None, 1, 1, 1, 10, 1.0, None, None, None, None, None, None,
                               None, None) == G.SPEC_ERR_ARG
     assert lib.spec_verify_destroy(None) == G.SPEC_OK

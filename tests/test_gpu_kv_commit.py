@@ -41,8 +41,11 @@ def _paths(rng, parent):
 @pytest.mark.parametrize("cache", [K.SAME, K.FP8_E4M3, K.FP8_E5M2])
 @pytest.mark.parametrize("layout", [K.NHD, K.HND])
 @pytest.mark.parametrize("D", [128, 36])
-def test_kv_commit_matches_oracle(h, src, cache, layout, D):
-    rng = np.random.default_rng(hash((src, cache, layout, D)) % 2**32)
+@pytest.mark.parametrize("scales", ["tensor", "token"])
+def test_kv_commit_matches_oracle(h, src, cache, layout, D, scales):
+    if cache == K.SAME and scales == "token":
+        pytest.skip("scales apply to fp8 caches only")
+    rng = np.random.default_rng(hash((src, cache, layout, D, scales)) % 2**32)
     B, N, H, bs = 12, 16, 4, 16
     parent = np.stack([W.random_trie(rng, N, 6, 3) for _ in range(B)])
     kv, al = _paths(rng, parent)
@@ -73,7 +76,11 @@ def test_kv_commit_matches_oracle(h, src, cache, layout, D):
     tv = torch.from_numpy(vvals).to(TDT[src])
     kf, vf = tk.float().numpy(), tv.float().numpy()   # exact values of the source type
     shape = (num_blocks, bs, H, D) if layout == K.NHD else (num_blocks, H, bs, D)
-    ks, vs = 0.5, 2.0
+    if scales == "tensor":
+        ks, vs = 0.5, 2.0
+    else:   # one scale per source token, [B, N]
+        ks = (2.0 ** rng.uniform(-3, 3, (B, N))).astype(np.float32)
+        vs = (2.0 ** rng.uniform(-3, 3, (B, N))).astype(np.float32)
     if cache == K.SAME:
         ck0 = torch.full(shape, -1024.0, dtype=TDT[src])
         cv0 = ck0.clone()
@@ -86,8 +93,8 @@ def test_kv_commit_matches_oracle(h, src, cache, layout, D):
                                            table, pos, cache_kind=cache, k_scale=ks, v_scale=vs)
     gk, gv = ck0.to(DEV), cv0.to(DEV)
     st = torch.full((B,), -7, dtype=torch.int32, device=DEV)
-    scale_k = torch.tensor([ks], device=DEV)
-    scale_v = torch.tensor([vs], device=DEV)
+    scale_k = torch.tensor(np.atleast_1d(ks), dtype=torch.float32, device=DEV)
+    scale_v = torch.tensor(np.atleast_1d(vs), dtype=torch.float32, device=DEV)
     G.spec_kv_commit(h, tk.to(DEV), tv.to(DEV), torch.from_numpy(kv).to(DEV),
                      torch.from_numpy(al).to(DEV), gk, gv, layout,
                      torch.from_numpy(table).to(DEV), torch.from_numpy(pos).to(DEV),

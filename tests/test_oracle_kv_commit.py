@@ -61,3 +61,43 @@ def test_failed_request_and_bad_slot():
     assert st.tolist() == [0, K.BAD_SLOT]
     assert (ck[0] == 0).all() and (ck[1] == 0).all()          # request 0 wrote nothing
     assert (ck[3] == 1).all()                                    # positions 2, 3 -> block 3
+
+
+def test_per_token_scales_hand_worked():
+    """Per-token scales: slot j of the path divides by the scale of its source token (b, node).
+    Chain 0 -> 1 -> 2 with K values 1.0, 3.0, 10.0 and per-node scales 0.5, 2.0, 4.0: the cache
+    holds e4m3(2.0) = 0x40, e4m3(1.5) = 0x3C, e4m3(2.5) = 0x42 (bias 7: 2.0 = 2^1 -> 0x40,
+    1.5 = 1.1b * 2^0 -> 0x3C, 2.5 = 1.01b * 2^1 -> 0x42); V with a scalar scale of 1 for
+    comparison: 1.0 -> 0x38, 3.0 -> 0x44, 10.0 -> 0x52."""
+    vals = np.array([1.0, 3.0, 10.0], np.float32).reshape(1, 3, 1, 1)
+    kv = np.array([[0, 1, 2]], np.int32)
+    al = np.array([2], np.int32)
+    table = np.array([[0]], np.int32)
+    pos = np.array([0], np.int32)
+    cache = np.zeros((1, 4, 1, 1), np.uint8)
+    ks = np.array([[0.5, 2.0, 4.0]], np.float32)
+    ck, _, st = K.kv_commit(vals, vals, kv, al, cache, cache, K.NHD, 4, table, pos,
+                            cache_kind=K.FP8_E4M3, k_scale=ks, v_scale=1.0)
+    assert st.tolist() == [0]
+    assert ck[0, :3, 0, 0].tolist() == [0x40, 0x3C, 0x42]
+    _, cv, _ = K.kv_commit(vals, vals, kv, al, cache, cache, K.NHD, 4, table, pos,
+                           cache_kind=K.FP8_E4M3, k_scale=ks, v_scale=1.0)
+    assert cv[0, :3, 0, 0].tolist() == [0x38, 0x44, 0x52]
+
+
+def test_uniform_per_token_scales_equal_the_scalar():
+    rng = np.random.default_rng(3)
+    B, N, H, D = 3, 5, 2, 4
+    src = (rng.standard_normal((B, N, H, D)) * 5).astype(np.float32)
+    kv = np.tile(np.arange(N, dtype=np.int32), (B, 1))
+    al = np.full(B, N - 1, np.int32)
+    table = np.arange(B * 2, dtype=np.int32).reshape(B, 2)
+    pos = np.zeros(B, np.int32)
+    cache = np.zeros((B * 2, 4, H, D), np.uint8)
+    a = K.kv_commit(src, src, kv, al, cache, cache, K.NHD, 4, table, pos, cache_kind=K.FP8_E5M2,
+                    k_scale=0.75, v_scale=3.0)
+    b = K.kv_commit(src, src, kv, al, cache, cache, K.NHD, 4, table, pos, cache_kind=K.FP8_E5M2,
+                    k_scale=np.full((B, N), 0.75, np.float32),
+                    v_scale=np.full((B, N), 3.0, np.float32))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
