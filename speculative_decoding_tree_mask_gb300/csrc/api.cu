@@ -28,6 +28,7 @@ struct spec_ctx {
     float *m = nullptr, *s = nullptr, *pc = nullptr, *mq = nullptr, *sq = nullptr,
           *qc = nullptr;
     int32_t *arg = nullptr, *flags = nullptr, *dflags = nullptr;
+    float2 *chunk = nullptr;              // row-chunk partials of the target rows
     const int32_t *n_active = nullptr;   // node budget set by spec_set_node_budget
     bool prof = false;
     bool ev_ready = false;
@@ -179,18 +180,19 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
     h->max_N = max_N;
     h->max_V = max_V;
     const size_t rows = (size_t)max_B * max_N;
-    const size_t bytes = rows * 9 * 4;
+    const size_t bytes = rows * (9 * 4 + kRowChunks * sizeof(float2));
     if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return SPEC_ERR_WORKSPACE;
     }
-    char *p = static_cast<char *>(h->ws);
+    char *p = static_cast<char *>(h->ws);   // cudaMalloc: 256-byte aligned
     auto take = [&](size_t n) {
         char *q = p;
         p += n;
         return q;
     };
+    h->chunk = reinterpret_cast<float2 *>(take(rows * kRowChunks * sizeof(float2)));
     h->m = reinterpret_cast<float *>(take(rows * 4));
     h->s = reinterpret_cast<float *>(take(rows * 4));
     h->pc = reinterpret_cast<float *>(take(rows * 4));
@@ -291,12 +293,14 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     rp.flags = h->flags;
     rp.pc = h->pc;
     rp.n_active = h->n_active;
+    rp.chunk = h->chunk;
     rc = timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
     if (rc != SPEC_OK) return rc;
 
     if (dense) {
         RowStatsParams dp = rp;
         dp.x = draft;
+        dp.chunk = nullptr;   // partials are kept for the target rows only
         dp.skip_leaves = 1;
         dp.flags = h->dflags;
         dp.pc = h->qc;
@@ -337,6 +341,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     wp.dflags = h->dflags;
     wp.out = out;
     wp.n_active = h->n_active;
+    wp.chunk = draft_kind == SPEC_DRAFT_POINT ? h->chunk : nullptr;
     return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
 }
 

@@ -130,17 +130,20 @@ __device__ __forceinline__ Part merge(Part x, Part y, float k) {
     return r;
 }
 
+// The partial of lane (lane ^ o).
+__device__ __forceinline__ Part shfl_part(const Part &p, int o) {
+    Part q;
+    q.m = shfl_xor(p.m, o);
+    q.s = shfl_xor(p.s, o);
+    q.arg = shfl_xor(p.arg, o);
+    q.flags = shfl_xor(p.flags, o);
+    return q;
+}
+
 template <int MODE>
 __device__ __forceinline__ Part warp_merge(Part p, float k) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Part q;
-        q.m = shfl_xor(p.m, o);
-        q.s = shfl_xor(p.s, o);
-        q.arg = shfl_xor(p.arg, o);
-        q.flags = shfl_xor(p.flags, o);
-        p = merge<MODE>(p, q, k);
-    }
+    for (int o = 16; o > 0; o >>= 1) p = merge<MODE>(p, shfl_part(p, o), k);
     return p;
 }
 

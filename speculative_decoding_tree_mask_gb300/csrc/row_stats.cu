@@ -12,7 +12,12 @@
 // times per thread) the sum is rescaled. Elements are visited in increasing index order per
 // thread, so a strict '>' keeps the lowest index; partial results merge lowest-index-first.
 // The stream is HBM-bound: 16-byte read-only loads, 4 in flight per thread, 256 threads per
-// CTA and 6 CTAs per SM (24 KiB of loads in flight per CTA).
+// CTA and 6 CTAs per SM (16 KiB of loads in flight per CTA).
+// The CTA splits the row into kRowChunks contiguous chunks, each streamed by its own group of
+// warps (threads interleaved, so one load instruction of a group covers contiguous memory).
+// For 16-byte aligned rows the chunks start on 256-element sub-tile boundaries, and in
+// sampling mode each chunk's (max, sum) is stored: the walk then locates the chunk holding
+// its inverse-CDF draw from these partials and re-reads only that chunk.
 
 #include <cfloat>
 
@@ -28,6 +33,8 @@ using namespace rowpass;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
+constexpr int kGroup = kThreads / kRowChunks;        // threads per chunk
+constexpr int kWarpsPerGroup = kWarps / kRowChunks;
 
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P) {
@@ -81,31 +88,35 @@ __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P
     a.arg = kNone;
     a.flags = 0;
 
-    // Split the row into a scalar head up to 16-byte alignment, vectors, and a scalar tail.
+    // Split the row into a scalar head up to 16-byte alignment, vectors, and a scalar tail;
+    // thread group g takes vectors [row_chunk_vec(g), row_chunk_vec(g + 1)), group 0 the head
+    // and the last group the tail.
     const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
     int64_t head = (int64_t)((16 - (addr & 15)) & 15) / kEsz;
     if (head > V) head = V;
-    const int64_t nvec = (V - head) / kEpv;
-    const int64_t tail0 = head + nvec * kEpv;
-    if (tid < head) proc_scalar<MODE>(a, load_elem<DT>(rowp, tid), tid, k);
+    const int nv = (int)((V - head) / kEpv);
+    const int64_t tail0 = head + (int64_t)nv * kEpv;
+    const bool aligned = head == 0;
+    const int g = tid / kGroup, gt = tid - g * kGroup;
+    const int v1 = row_chunk_vec(g + 1, nv, V, aligned, kEpv);
+    if (g == 0 && gt < head) proc_scalar<MODE>(a, load_elem<DT>(rowp, gt), gt, k);
 
     const uint4 *vb = reinterpret_cast<const uint4 *>(rowp + head * kEsz);
-    const int nv = (int)nvec;
-    int i = tid;
-    for (; i + (kUnroll - 1) * kThreads < nv; i += kUnroll * kThreads) {
+    int i = row_chunk_vec(g, nv, V, aligned, kEpv) + gt;
+    for (; i + (kUnroll - 1) * kGroup < v1; i += kUnroll * kGroup) {
         uint4 w[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kThreads);
+        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kGroup);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int e0 = (int)head + (i + u * kThreads) * kEpv;
+            const int e0 = (int)head + (i + u * kGroup) * kEpv;
             if (DT == 1)
                 proc_bf16<MODE>(a, w[u], e0, k);
             else
                 proc_f32<MODE>(a, w[u], e0, k);
         }
     }
-    for (; i < nv; i += kThreads) {
+    for (; i < v1; i += kGroup) {
         const uint4 w = ldg_stream(vb + i);
         const int e0 = (int)head + i * kEpv;
         if (DT == 1)
@@ -113,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P
         else
             proc_f32<MODE>(a, w, e0, k);
     }
-    if (tail0 + tid < V) {
-        const int idx = (int)(tail0 + tid);
+    if (g == kRowChunks - 1 && tail0 + gt < V) {
+        const int idx = (int)(tail0 + gt);
         proc_scalar<MODE>(a, load_elem<DT>(rowp, idx), idx, k);
     }
 
@@ -125,7 +136,13 @@ __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P
     __syncthreads();
     if (warp != 0) return;
     p = lane < kWarps ? sh_part[lane] : Part{-INFINITY, 0.f, kNone, 0};
-    p = warp_merge<MODE>(p, k);
+    // warps of one chunk first (consecutive lanes), then across chunks
+#pragma unroll
+    for (int o = 1; o < kWarpsPerGroup; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
+    if (MODE == ROW_SAMPLE && P.chunk && aligned && lane < kWarps && lane % kWarpsPerGroup == 0)
+        P.chunk[(size_t)row * kRowChunks + lane / kWarpsPerGroup] = make_float2(p.m, p.s);
+#pragma unroll
+    for (int o = kWarpsPerGroup; o < 32; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
 
     if (MODE != ROW_PROBS) {
         if (p.m == INFINITY) p.flags |= F_POSINF;

@@ -11,6 +11,33 @@ namespace specv {
 constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)
 
 enum RowMode { ROW_GREEDY = 0, ROW_SAMPLE = 1, ROW_PROBS = 2 };
+
+// Row chunks: the row-statistics stream splits every row into kRowChunks contiguous pieces
+// and, for sampling rows that start 16-byte aligned, stores each piece's (max, sum) so that
+// the inverse-CDF bonus re-reads one piece instead of the row.
+#ifndef SPEC_ROW_CHUNKS
+#define SPEC_ROW_CHUNKS 8
+#endif
+constexpr int kRowChunks = SPEC_ROW_CHUNKS;
+static_assert(kRowChunks == 1 || kRowChunks == 2 || kRowChunks == 4 || kRowChunks == 8,
+              "row chunks: a power of two that divides the 8 warps of the stream");
+constexpr int kSubTile = 256;   // elements per sub-tile of the walk's bonus search
+
+// First vector of chunk c (c = 0..kRowChunks) of a row of nv 16-byte vectors holding epv
+// elements each. Aligned rows cut on sub-tile boundaries (as balanced as whole sub-tiles
+// allow), so chunk c covers elements [chunk_sub(c) * kSubTile, chunk_sub(c + 1) * kSubTile)
+// clipped to V; other rows split the vectors evenly.
+__host__ __device__ __forceinline__ int row_chunk_sub(int c, int64_t V) {
+    const int64_t nsub = (V + kSubTile - 1) / kSubTile;
+    return (int)(nsub * c / kRowChunks);
+}
+__host__ __device__ __forceinline__ int row_chunk_vec(int c, int nv, int64_t V, bool aligned,
+                                                      int epv) {
+    if (c >= kRowChunks) return nv;
+    if (!aligned) return (int)((int64_t)nv * c / kRowChunks);
+    const int64_t v = (int64_t)row_chunk_sub(c, V) * (kSubTile / epv);
+    return v < nv ? (int)v : nv;
+}
 enum DraftKind { DRAFT_POINT = 0, DRAFT_PROBS_F32 = 1, DRAFT_LOGITS = 2 };
 
 // Row statistics over `rows` rows of V elements (see spec_row_stats in spec_verify.h).
@@ -30,6 +57,7 @@ struct RowStatsParams {
     float *pc;               // child_prob output (indexed by child row); may be null
     int pc_normalized;       // 1: pc = e_t / S (probability); 0: pc = e_t (walk input)
     const int32_t *n_active = nullptr;   // per-request node budget [B]; null = all N rows
+    float2 *chunk = nullptr;   // sampling: (max, sum) of each row chunk [rows, kRowChunks]
 };
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);
@@ -88,6 +116,7 @@ struct SampleWalkParams {
     int lazy;                     // 1: no row statistics precomputed; stream visited rows only
     WalkOutputs out;
     const int32_t *n_active = nullptr;
+    const float2 *chunk = nullptr;   // row-chunk partials of the target rows (eager, may be null)
 };
 
 // KV commit of the accepted path into a paged cache (see spec_kv_commit).

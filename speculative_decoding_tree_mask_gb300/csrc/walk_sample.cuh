@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSub = 256;   // elements per sub-tile: 32 lanes x 8
+constexpr int kSub = kSubTile;   // elements per sub-tile: 32 lanes x 8
 
 enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z, CMD_STATS };
 
@@ -60,6 +60,8 @@ struct Smem {
     double total;
     double wtot[kWarps];
     int haskids;                       // lazy statistics: the node has children
+    int cpick;                         // eager point bonus: chosen row chunk (-1: none)
+    double ctau;                       // ... and tau relative to the chunk's start
     int subsum_node;                   // node whose rescaled sub-tile sums are in subsum[]
     int wflag[kWarps];
     rowpass::Part part[kWarps], part_out;
@@ -202,21 +204,23 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
 
 // ---- one pass over the node's residual ----------------------------------------------------
 
-// Every warp sums its sub-tiles into subsum[] (one warp scan per 256 elements); the CTA total
-// lands in sm.total. All threads call it; it ends synchronised.
+// Every warp sums its sub-tiles of [jlo, jhi) (default: the whole row) into subsum[] (one warp
+// scan per 256 elements); the total lands in sm.total. All threads call it; it ends
+// synchronised.
 template <int DT, int DK, int DDT>
-__device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum) {
+__device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0,
+                              int jhi = INT_MAX) {
     // sub-tiles in flight per warp (32 registers of raw loads)
     constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : 2;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nsub = (c.V + kSub - 1) / kSub;
+    const int nsub = min((c.V + kSub - 1) / kSub, jhi);
     const bool vec = c.zvec && (DK == DRAFT_POINT || !c.useq || c.dvec);
-    const int nfull = vec ? c.V / kSub : 0;
+    const int nfull = min(vec ? c.V / kSub : 0, nsub);
     KSum wsum;
     int rc = 0;
 
-    for (int j0 = warp; j0 < nfull; j0 += kWarps * U) {
+    for (int j0 = jlo + warp; j0 < nfull; j0 += kWarps * U) {
         uint4 za[U], zb[U], da[U], db[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -246,7 +250,7 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum) {
         }
     }
     // Ragged last sub-tile, or every sub-tile of a row that is not 16-byte aligned.
-    for (int j = nfull + warp; j < nsub; j += kWarps) {
+    for (int j = max(nfull, jlo) + warp; j < nsub; j += kWarps) {
         float r[8];
         residual8_any<DT, DK, DDT>(c, sm, j, lane, rc, r);
         const float incl = warp_incl_scan(sum8(r));
@@ -267,14 +271,15 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum) {
     __syncthreads();
 }
 
-// Largest token with r > 0 (warp 0), from the stored sub-tile sums: the fallback when rounding
-// leaves tau at the very end of the row. -1 if the residual is zero everywhere.
+// Largest token with r > 0 in sub-tiles [jlo, jhi) (warp 0), from the stored sub-tile sums:
+// the fallback when rounding leaves tau at the very end of the range. -1 if the residual is
+// zero there.
 template <int DT, int DK, int DDT>
-__device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum) {
+__device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum, int jlo,
+                             int jhi) {
     const int lane = threadIdx.x & 31;
-    const int nsub = (c.V + kSub - 1) / kSub;
     int jl = -1;
-    for (int j = lane; j < nsub; j += 32)
+    for (int j = jlo + lane; j < jhi; j += 32)
         if (subsum[j] > 0.f) jl = j;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) jl = max(jl, shfl_xor(jl, o));
@@ -291,16 +296,19 @@ __device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum) 
     return lk;
 }
 
-// Inverse CDF over the stored sub-tile sums (warp 0): the bonus token for uniform u, or -1
-// when the residual sums to zero.
+// Inverse CDF over the stored sub-tile sums of [jlo, jhi) (warp 0; default: the whole row):
+// the bonus token for tau = u * (sum of the range), or for the given tau_abs >= 0; -1 when the
+// residual sums to zero there.
 template <int DT, int DK, int DDT>
-__device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, float u) {
+__device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, float u,
+                            int jlo = 0, int jhi = -1, double tau_abs = -1.0) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const int nsub = (c.V + kSub - 1) / kSub;
+    if (jhi < 0) jhi = (c.V + kSub - 1) / kSub;
+    const int nsub = jhi - jlo;
     // level 1: every lane sums a contiguous chunk of sub-tiles; scan the chunk totals
     const int cs = (nsub + 31) / 32;
-    const int lo = min(lane * cs, nsub), hi = min(lo + cs, nsub);
+    const int lo = jlo + min(lane * cs, nsub), hi = jlo + min(lane * cs + cs, nsub);
     KSum chunk;
     for (int j = lo; j < hi; ++j) chunk.add(subsum[j]);
     const double incl = warp_incl_scan_d(chunk.value());
@@ -308,9 +316,9 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
     if (!(S > 0.0)) return -1;
     double excl = __shfl_up_sync(full, incl, 1);
     if (lane == 0) excl = 0.0;
-    const double tau = (double)u * S;
+    const double tau = tau_abs >= 0.0 ? tau_abs : (double)u * S;
     const unsigned ball = __ballot_sync(full, incl > tau);
-    if (ball == 0) return last_positive<DT, DK, DDT>(c, sm, subsum);
+    if (ball == 0) return last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
     const int owner = __ffs(ball) - 1;
     const int olo = __shfl_sync(full, lo, owner), ohi = __shfl_sync(full, hi, owner);
     double base = __shfl_sync(full, excl, owner);
@@ -340,7 +348,7 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
         js = jlast;
         pref = plast;
     }
-    if (js < 0) return last_positive<DT, DK, DDT>(c, sm, subsum);
+    if (js < 0) return last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
 
     // level 3: re-read sub-tile js; scan its 32 lanes x 8 elements (the pass's arithmetic)
     const float tr = (float)(tau - pref);
@@ -370,9 +378,48 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
     if (hitk < 0) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lastk = max(lastk, shfl_xor(lastk, o));
-        hitk = lastk >= 0 ? lastk : last_positive<DT, DK, DDT>(c, sm, subsum);
+        hitk = lastk >= 0 ? lastk : last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
     }
     return hitk;
+}
+
+// Point drafts, eager: choose the row chunk holding the bonus draw from the row-statistics
+// chunk partials (warp 0). The residual mass of chunk q is its sum rescaled to the row max
+// minus e_t of the rejected tokens inside it; tau = u * (total). Stores the chunk (-1: none
+// has mass) and tau relative to the chunk's start in sm.cpick / sm.ctau.
+__device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, float u) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    double M = 0.0;
+    if (lane < kRowChunks) {
+        const float2 pq = part[lane];
+        const int lo = row_chunk_sub(lane, c.V) * kSub;
+        const int hi = lane == kRowChunks - 1 ? c.V : row_chunk_sub(lane + 1, c.V) * kSub;
+        double mq = pq.y > 0.f ? (double)(pq.y * ex2((pq.x + c.negm) * c.k)) : 0.0;
+        for (int i = 0; i < sm.nR; ++i) {
+            const int t = sm.R[i];
+            if (t >= lo && t < hi) mq -= (double)sm.RE[i];
+        }
+        M = mq > 0.0 ? mq : 0.0;
+    }
+    const double incl = warp_incl_scan_d(M);
+    const double S = __shfl_sync(full, incl, 31);
+    double excl = __shfl_up_sync(full, incl, 1);
+    if (lane == 0) excl = 0.0;
+    int pick = -1;
+    double tau = 0.0;
+    if (S > 0.0) {
+        tau = (double)u * S;
+        const unsigned hit = __ballot_sync(full, lane < kRowChunks && incl > tau);
+        const unsigned pos = __ballot_sync(full, lane < kRowChunks && M > 0.0);
+        pick = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        if (pick >= 0) tau = fmax(tau - __shfl_sync(full, excl, pick), 0.0);
+    }
+    if (lane == 0) {
+        sm.cpick = pick;
+        sm.ctau = tau;
+    }
+    __syncwarp();
 }
 
 // ---- the walk (warp 0) ---------------------------------------------------------------------
@@ -809,6 +856,30 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     if (cmd == CMD_BONUS) {
         const float ub = sm.u[N];
         bool drawn = false;
+        if (!LAZY && DK == DRAFT_POINT && P.chunk != nullptr) {
+            // One chunk instead of the row: locate the chunk from the row-statistics partials,
+            // then sum and search only its sub-tiles. Rows that are not 16-byte aligned have
+            // no partials.
+            const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
+            if (c.zvec) {
+                if (warp == 0)
+                    chunk_pick(c, sm, P.chunk + (base + sm.node) * kRowChunks, ub);
+                __syncthreads();
+                const int q = sm.cpick;
+                if (q >= 0) {
+                    const int jlo = row_chunk_sub(q, c.V), jhi = row_chunk_sub(q + 1, c.V);
+                    if (tid == 0) sm.subsum_node = -1;
+                    residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
+                    if (warp == 0) {
+                        const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
+                                                                sm.ctau);
+                        if (lane == 0) sm.bonus = v;
+                    }
+                    __syncthreads();
+                    drawn = sm.bonus >= 0;
+                }
+            }
+        }
         if (LAZY && DK == DRAFT_POINT && sm.subsum_node == sm.node) {
             // Single pass: the stored sub-tile sums of this row minus the rejected tokens.
             if (tid == 0)
