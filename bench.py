@@ -90,20 +90,28 @@ def peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+def source_sha(files) -> str:
+    """Hash of the kernel's source files (the .cu and every header it includes)."""
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "speculative_decoding_tree_mask_gb300", "csrc", name),
+                  "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel_file: str):
-    """Per-launch DRAM bytes of the row-stats kernel from the committed ncu summary, if the
-    kernel source is unchanged since the capture; else None."""
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if none of the
+    kernel's source files changed since the capture; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "speculative_decoding_tree_mask_gb300", "csrc", kernel_file)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel_file)
     if not rec:
         return None
-    with open(src, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if rec.get("source_sha") == sha else None
+    return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha(rec["sources"]) \
+        else None
 
 
 class ClockSampler:

@@ -30,14 +30,21 @@ namespace {
 
 using namespace rowpass;
 
+#ifndef SPEC_ROW_UNROLL
+#define SPEC_ROW_UNROLL 4   // 16-byte loads in flight per thread
+#endif
+#ifndef SPEC_ROW_MIN_CTAS
+#define SPEC_ROW_MIN_CTAS 6   // resident CTAs per SM the register budget is sized for
+#endif
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = SPEC_ROW_UNROLL;
 constexpr int kGroup = kThreads / kRowChunks;        // threads per chunk
 constexpr int kWarpsPerGroup = kWarps / kRowChunks;
 
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(RowStatsParams P) {
+__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(RowStatsParams P) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
     const int row = blockIdx.x;
