@@ -402,7 +402,7 @@ def bench_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic (seeded random tries and N(0,3) logits)",
+                "dtype": "f32", "data": "synthetic (seeded random tries and N(0,3) logits)",
                 "config": config_of(w, world),
                 "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
                 "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
