@@ -161,12 +161,39 @@ int oracle_row_softmax(const void *row, int dtype, int64_t V, double T, double *
     return 0;
 }
 
+/* Half-width, relative to S, of the window of draws reported beside every inverse CDF: the
+ * tolerance below which the comparisons accept a different token from an arithmetic that
+ * rounds the running sums differently. */
+#define OR_CDF_WINDOW 1e-6
+
 /* InvCDF(r, u): with S = sum r and tau = u*S, the smallest v whose running sum exceeds
  * tau; if rounding leaves none, the largest v with r[v] > 0. The margin is the distance of
  * tau to the nearer end of the chosen interval, over S (0 on the fallback). *alt is the token
  * with r > 0 on the other side of that nearer end (v itself if there is none): the draw an
- * arithmetic that rounds the running sums differently may make when the margin is tiny. */
-static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin, int64_t *alt) {
+ * arithmetic that rounds the running sums differently may make when the margin is tiny.
+ * win[0..1] is the first and last token with r > 0 whose interval [C(v) - r(v), C(v))
+ * comes within OR_CDF_WINDOW * S of tau: every token such an arithmetic can draw when its
+ * tau and running sums are off by less than that (tokens of tiny mass can put several of
+ * them inside the window). */
+static void cdf_window(const double *r, int64_t V, double S, double tau, int64_t drawn,
+                       int64_t *win) {
+    double delta = OR_CDF_WINDOW * S, C = 0.0;
+    win[0] = -1;
+    win[1] = -1;
+    for (int64_t v = 0; v < V; v++) {
+        double Cprev = C;
+        C += r[v];
+        if (!(r[v] > 0.0)) continue;
+        if (Cprev >= tau + delta) break;
+        if (win[0] < 0 && C > tau - delta) win[0] = v;
+        win[1] = v;
+    }
+    if (win[0] < 0 || win[0] > drawn) win[0] = drawn;
+    if (win[1] < drawn) win[1] = drawn;
+}
+
+static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin, int64_t *alt,
+                       int64_t *win) {
     double S = 0.0;
     for (int64_t v = 0; v < V; v++) S += r[v];
     double tau = u * S;
@@ -191,6 +218,7 @@ static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin, int
                         break;
                     }
             }
+            cdf_window(r, V, S, tau, v, win);
             return v;
         }
     }
@@ -198,15 +226,17 @@ static int64_t inv_cdf(const double *r, int64_t V, double u, double *margin, int
     for (int64_t v = V - 1; v >= 0; v--)
         if (r[v] > 0) {
             *alt = v;
+            cdf_window(r, V, S, tau, v, win);
             return v;
         }
     *alt = V - 1;
+    win[0] = win[1] = V - 1;
     return V - 1;
 }
 
-int64_t oracle_inv_cdf(const double *r, int64_t V, double u, double *margin) {
+int64_t oracle_inv_cdf(const double *r, int64_t V, double u, double *margin, int64_t *win) {
     int64_t alt;
-    return inv_cdf(r, V, u, margin, &alt);
+    return inv_cdf(r, V, u, margin, &alt, win);
 }
 
 /* ---- per-request outputs ------------------------------------------------------------------ */
@@ -323,7 +353,7 @@ typedef struct {
 static int32_t sample_point(const void *logits, int dtype, int b, int N, int64_t V, double T,
                             const int32_t *tok, const int32_t *par, const float *u,
                             scratch s, int *path, int *L_out, double *dmargin, double *cmargin,
-                            int32_t *calt) {
+                            int32_t *calt, int32_t *cwin) {
     int node = 0, L = 0;
     double *p = s.p, *r = s.r;
     char *inR = (char *)s.tmp; /* V bytes */
@@ -357,10 +387,12 @@ static int32_t sample_point(const void *logits, int dtype, int b, int N, int64_t
     }
     for (int64_t v = 0; v < V; v++) r[v] = inR[v] ? 0.0 : p[v];
     double cm;
-    int64_t alt;
-    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt);
+    int64_t alt, win[2];
+    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt, win);
     *cmargin = cm;
     *calt = (int32_t)alt;
+    cwin[0] = (int32_t)win[0];
+    cwin[1] = (int32_t)win[1];
     *L_out = L;
     return (int32_t)bonus;
 }
@@ -396,7 +428,7 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
                             const int32_t *tok, const int32_t *par, const void *draft,
                             int draft_kind, int draft_dtype, const float *u, scratch s,
                             int *path, int *L_out, double *dmargin, double *cmargin,
-                            int32_t *degenerate, int32_t *calt) {
+                            int32_t *degenerate, int32_t *calt, int32_t *cwin) {
     int node = 0, L = 0;
     double *p = s.p, *r = s.r, *q = s.q;
     for (;;) {
@@ -441,10 +473,12 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
         node = next;
     }
     double cm;
-    int64_t alt;
-    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt);
+    int64_t alt, win[2];
+    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt, win);
     *cmargin = cm;
     *calt = (int32_t)alt;
+    cwin[0] = (int32_t)win[0];
+    cwin[1] = (int32_t)win[1];
     *L_out = L;
     return (int32_t)bonus;
 }
@@ -454,14 +488,16 @@ static int32_t sample_dense(const void *logits, int dtype, int b, int N, int64_t
  * not the walk consumes the slot). decision_margin[b] is the smallest |u - r(x)/q(x)| over
  * the tests taken (= |u*q - r|/q, never below |u*q - r| as q <= 1; +inf if no test),
  * cdf_margin[b] the bonus draw's margin, cdf_alt[b] the token across the nearer boundary of
- * the drawn interval, degenerate[b] the number of degenerate dense residuals. */
+ * the drawn interval, cdf_window[b][0..1] the first and last token an arithmetic within
+ * OR_CDF_WINDOW of tau can draw (see inv_cdf; -1 without a draw), degenerate[b] the number
+ * of degenerate dense residuals. */
 int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
                          const int32_t *draft_token, const int32_t *parent, const void *draft,
                          int draft_kind, int draft_dtype, double T, const float *uniforms,
                          int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
                          int32_t *bonus, int32_t *status, double *decision_margin,
-                         double *cdf_margin, int32_t *cdf_alt, int32_t *degenerate,
-                         int nthreads) {
+                         double *cdf_margin, int32_t *cdf_alt, int32_t *cdf_window,
+                         int32_t *degenerate, int nthreads) {
     if (B < 0 || N < 1 || N > 64 || V < 1 || (dtype != OR_F32 && dtype != OR_BF16)) return -1;
     if (!(T >= 0.0) || isinf(T)) return -1;
     if (draft_kind != OR_DRAFT_POINT && draft_kind != OR_DRAFT_PROBS_F32 &&
@@ -480,6 +516,7 @@ int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
         decision_margin[b] = INFINITY;
         cdf_margin[b] = INFINITY;
         cdf_alt[b] = -1;
+        cdf_window[2 * b] = cdf_window[2 * b + 1] = -1;
         degenerate[b] = 0;
         if (T == 0.0) {
             greedy_one(logits, dtype, b, N, V, tok, par, o);
@@ -502,11 +539,13 @@ int oracle_verify_sample(const void *logits, int dtype, int B, int N, int64_t V,
         int32_t res;
         if (draft_kind == OR_DRAFT_POINT)
             res = sample_point(logits, dtype, b, N, V, T, tok, par, u, s, path, &L,
-                               &decision_margin[b], &cdf_margin[b], &cdf_alt[b]);
+                               &decision_margin[b], &cdf_margin[b], &cdf_alt[b],
+                               &cdf_window[2 * b]);
         else
             res = sample_dense(logits, dtype, b, N, V, T, tok, par, draft, draft_kind,
                                draft_dtype, u, s, path, &L, &decision_margin[b],
-                               &cdf_margin[b], &degenerate[b], &cdf_alt[b]);
+                               &cdf_margin[b], &degenerate[b], &cdf_alt[b],
+                               &cdf_window[2 * b]);
         if (res < 0)
             write_failed(o, b, N, -res);
         else

@@ -55,11 +55,11 @@ class Oracle:
         lib.oracle_build_mask.argtypes = [P, i32, i32, P, P, P]
         lib.oracle_row_stats.argtypes = [P, i32, i64, f64, P, P, P, P]
         lib.oracle_row_softmax.argtypes = [P, i32, i64, f64, P]
-        lib.oracle_inv_cdf.argtypes = [P, i64, f64, P]
+        lib.oracle_inv_cdf.argtypes = [P, i64, f64, P, P]
         lib.oracle_inv_cdf.restype = i64
         lib.oracle_verify_greedy.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, P, P, i32]
         lib.oracle_verify_sample.argtypes = [P, i32, i32, i32, i64, P, P, P, i32, i32, f64,
-                                             P, P, P, P, P, P, P, P, P, P, i32]
+                                             P, P, P, P, P, P, P, P, P, P, P, i32]
         lib.oracle_max_threads.restype = i32
         self.lib = lib
         self.path = path
@@ -100,10 +100,15 @@ class Oracle:
             raise ValueError("oracle_row_softmax rejected its arguments")
         return p
 
-    def inv_cdf(self, r: np.ndarray, u: float):
+    def inv_cdf(self, r: np.ndarray, u: float, window: bool = False):
+        """-> (token, margin), or (token, margin, (first, last token of the draw window))."""
         r = np.ascontiguousarray(r, dtype=np.float64)
         margin = ctypes.c_double()
-        v = self.lib.oracle_inv_cdf(_ptr(r), r.shape[0], float(u), ctypes.byref(margin))
+        win = np.zeros(2, np.int64)
+        v = self.lib.oracle_inv_cdf(_ptr(r), r.shape[0], float(u), ctypes.byref(margin),
+                                    _ptr(win))
+        if window:
+            return int(v), margin.value, (int(win[0]), int(win[1]))
         return int(v), margin.value
 
     @staticmethod
@@ -147,16 +152,18 @@ class Oracle:
         dm = np.zeros(B, np.float64)
         cm = np.zeros(B, np.float64)
         ca = np.zeros(B, np.int32)
+        cw = np.zeros((B, 2), np.int32)
         dg = np.zeros(B, np.int32)
         rc = self.lib.oracle_verify_sample(_ptr(logits), _dtype_code(logits), B, N, V,
                                            _ptr(tok), _ptr(par), _ptr(draft), int(draft_kind),
                                            ddt, float(temperature), _ptr(u), _ptr(al), _ptr(ot),
                                            _ptr(kv), _ptr(bo), _ptr(st), _ptr(dm), _ptr(cm),
-                                           _ptr(ca), _ptr(dg), int(nthreads))
+                                           _ptr(ca), _ptr(cw), _ptr(dg), int(nthreads))
         if rc != 0:
             raise ValueError("oracle_verify_sample rejected its arguments")
         return dict(accept_len=al, out_tokens=ot, kv_commit=kv, bonus=bo, status=st,
-                    decision_margin=dm, cdf_margin=cm, cdf_alt=ca, degenerate=dg)
+                    decision_margin=dm, cdf_margin=cm, cdf_alt=ca, cdf_lo=cw[:, 0].copy(),
+                    cdf_hi=cw[:, 1].copy(), degenerate=dg)
 
 
 _default: Oracle | None = None

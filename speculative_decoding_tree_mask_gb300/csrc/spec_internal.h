@@ -23,19 +23,23 @@ static_assert(kRowChunks == 1 || kRowChunks == 2 || kRowChunks == 4 || kRowChunk
               "row chunks: a power of two that divides the 8 warps of the stream");
 constexpr int kSubTile = 256;   // elements per sub-tile of the walk's bonus search
 
-// First vector of chunk c (c = 0..kRowChunks) of a row of nv 16-byte vectors holding epv
-// elements each. Aligned rows cut on sub-tile boundaries (as balanced as whole sub-tiles
-// allow), so chunk c covers elements [chunk_sub(c) * kSubTile, chunk_sub(c + 1) * kSubTile)
-// clipped to V; other rows split the vectors evenly.
-__host__ __device__ __forceinline__ int row_chunk_sub(int c, int64_t V) {
+// The lazy walks split the rows they stream into one chunk per warp of their 512 threads.
+constexpr int kLazyChunks = 16;
+
+// First vector of chunk c (c = 0..nc) of a row of nv 16-byte vectors holding epv elements
+// each, for a split into nc chunks. Aligned rows cut on sub-tile boundaries (as balanced as
+// whole sub-tiles allow), so chunk c covers elements
+// [row_chunk_sub(c) * kSubTile, row_chunk_sub(c + 1) * kSubTile) clipped to V; other rows
+// split the vectors evenly.
+__host__ __device__ __forceinline__ int row_chunk_sub(int c, int64_t V, int nc = kRowChunks) {
     const int64_t nsub = (V + kSubTile - 1) / kSubTile;
-    return (int)(nsub * c / kRowChunks);
+    return (int)(nsub * c / nc);
 }
 __host__ __device__ __forceinline__ int row_chunk_vec(int c, int nv, int64_t V, bool aligned,
-                                                      int epv) {
-    if (c >= kRowChunks) return nv;
-    if (!aligned) return (int)((int64_t)nv * c / kRowChunks);
-    const int64_t v = (int64_t)row_chunk_sub(c, V) * (kSubTile / epv);
+                                                      int epv, int nc = kRowChunks) {
+    if (c >= nc) return nv;
+    if (!aligned) return (int)((int64_t)nv * c / nc);
+    const int64_t v = (int64_t)row_chunk_sub(c, V, nc) * (kSubTile / epv);
     return v < nv ? (int)v : nv;
 }
 enum DraftKind { DRAFT_POINT = 0, DRAFT_PROBS_F32 = 1, DRAFT_LOGITS = 2 };

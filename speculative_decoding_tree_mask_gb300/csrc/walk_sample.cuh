@@ -62,7 +62,8 @@ struct Smem {
     int haskids;                       // lazy statistics: the node has children
     int cpick;                         // eager point bonus: chosen row chunk (-1: none)
     double ctau;                       // ... and tau relative to the chunk's start
-    int subsum_node;                   // node whose rescaled sub-tile sums are in subsum[]
+    int cpart_node;                    // lazy: node whose chunk partials are in cpart[]
+    float2 cpart[kLazyChunks];         // lazy: (max, sum) of each chunk of that node's row
     int wflag[kWarps];
     rowpass::Part part[kWarps], part_out;
 };
@@ -383,19 +384,23 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
     return hitk;
 }
 
-// Point drafts, eager: choose the row chunk holding the bonus draw from the row-statistics
-// chunk partials (warp 0). The residual mass of chunk q is its sum rescaled to the row max
-// minus e_t of the rejected tokens inside it; tau = u * (total). Stores the chunk (-1: none
-// has mass) and tau relative to the chunk's start in sm.cpick / sm.ctau.
-__device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, float u) {
+// Point drafts: choose the row chunk holding the bonus draw from the chunk partials of the
+// stop row (warp 0). The residual mass of chunk q is its sum rescaled to the row max minus
+// e_t of the rejected tokens inside it; tau = u * (total). Stores the chunk and tau relative
+// to the chunk's start in sm.cpick / sm.ctau. The partials carry float32 rounding of the whole
+// row's mass, so when the rejected tokens held half of it or more, that rounding could move
+// tau by more than the residual's own precision: then sm.cpick = -1 and the caller sums the
+// residual over the whole row instead (as it does when no chunk has mass).
+__device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, float u) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    double M = 0.0;
-    if (lane < kRowChunks) {
+    double P = 0.0, M = 0.0;
+    if (lane < nc) {
         const float2 pq = part[lane];
-        const int lo = row_chunk_sub(lane, c.V) * kSub;
-        const int hi = lane == kRowChunks - 1 ? c.V : row_chunk_sub(lane + 1, c.V) * kSub;
-        double mq = pq.y > 0.f ? (double)(pq.y * ex2((pq.x + c.negm) * c.k)) : 0.0;
+        const int lo = row_chunk_sub(lane, c.V, nc) * kSub;
+        const int hi = lane == nc - 1 ? c.V : row_chunk_sub(lane + 1, c.V, nc) * kSub;
+        P = pq.y > 0.f ? (double)(pq.y * ex2((pq.x + c.negm) * c.k)) : 0.0;
+        double mq = P;
         for (int i = 0; i < sm.nR; ++i) {
             const int t = sm.R[i];
             if (t >= lo && t < hi) mq -= (double)sm.RE[i];
@@ -404,14 +409,17 @@ __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, float u) 
     }
     const double incl = warp_incl_scan_d(M);
     const double S = __shfl_sync(full, incl, 31);
+    double Ptot = P;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Ptot += __shfl_xor_sync(full, Ptot, o);
     double excl = __shfl_up_sync(full, incl, 1);
     if (lane == 0) excl = 0.0;
     int pick = -1;
     double tau = 0.0;
-    if (S > 0.0) {
+    if (S > 0.0 && S >= 0.5 * Ptot) {
         tau = (double)u * S;
-        const unsigned hit = __ballot_sync(full, lane < kRowChunks && incl > tau);
-        const unsigned pos = __ballot_sync(full, lane < kRowChunks && M > 0.0);
+        const unsigned hit = __ballot_sync(full, lane < nc && incl > tau);
+        const unsigned pos = __ballot_sync(full, lane < nc && M > 0.0);
         pick = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
         if (pick >= 0) tau = fmax(tau - __shfl_sync(full, excl, pick), 0.0);
     }
@@ -565,91 +573,76 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
     }
 }
 
-// Lazy walks, target row: one pass over 256-element sub-tiles (the bonus search's tiling)
-// gives every sub-tile's max M_j and S_j = sum 2^((z - M_j) k); the row's M = max M_j and
-// S = sum S_j 2^((M_j - M) k), and subsum[j] keeps S_j rescaled to M, so a bonus drawn from
-// this row re-reads one sub-tile instead of the whole row. Results land in sm.part_out
-// (m, s, flags). All threads call it; it ends synchronised.
+// Lazy walks, target row: the row-statistics stream's per-element arithmetic over one row,
+// split into kLazyChunks contiguous chunks, one per warp (lanes interleaved). Every
+// chunk's (max, sum) goes to sm.cpart, so a bonus drawn from this row sums only one chunk.
+// Results land in sm.part_out (m, s, flags). All threads call it; it ends synchronised.
 template <int DT>
-__device__ void lazy_row_pass(const char *row, int V, float k, Smem &sm, float *subsum,
-                              float *submax) {
-    constexpr int U = DT == 1 ? 4 : 2;   // sub-tiles in flight per warp
-    const unsigned full = 0xffffffffu;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nsub = (V + kSub - 1) / kSub;
-    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-    const int nfull = vec ? V / kSub : 0;
-    bool nan = false;
-
-    auto tile = [&](int j, const float (&x)[8]) {
-        float lm = -INFINITY;
+__device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
+    using namespace rowpass;
+    constexpr int kEsz = DT == 1 ? 2 : 4;
+    constexpr int kEpv = 16 / kEsz;
+    constexpr int kGroup = kThreads / kLazyChunks;   // threads per chunk
+    constexpr int kWpg = kWarps / kLazyChunks;       // warps per chunk
+    static_assert(kWpg >= 1 && kLazyChunks <= 32, "lazy chunks");
+    constexpr int kUnroll = 4;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    Acc a;
+    a.m = -INFINITY;
+    a.negm = 0.f;
+    a.s0 = a.s1 = 0.f;
+    a.arg = kNone;
+    a.flags = 0;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    int64_t head = (int64_t)((16 - (addr & 15)) & 15) / kEsz;
+    if (head > V) head = V;
+    const int nv = (int)((V - head) / kEpv);
+    const int64_t tail0 = head + (int64_t)nv * kEpv;
+    const bool aligned = head == 0;
+    const int g = tid / kGroup, gt = tid - g * kGroup;
+    const int v1 = row_chunk_vec(g + 1, nv, V, aligned, kEpv, kLazyChunks);
+    if (g == 0 && gt < head) proc_scalar<ROW_SAMPLE>(a, load_elem<DT>(row, gt), gt, k);
+    const uint4 *vb = reinterpret_cast<const uint4 *>(row + head * kEsz);
+    int i = row_chunk_vec(g, nv, V, aligned, kEpv, kLazyChunks) + gt;
+    for (; i + (kUnroll - 1) * kGroup < v1; i += kUnroll * kGroup) {
+        uint4 w[kUnroll];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            nan |= x[q] != x[q];
-            lm = fmaxf(lm, x[q]);
-        }
-        float wm = lm;
+        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kGroup);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(full, wm, o));
-        float sj = 0.f;
-        if (wm != -INFINITY && wm != INFINITY) {
-            const float negm = -wm;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sj += ex2((x[q] + negm) * k);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sj += __shfl_xor_sync(full, sj, o);
-        if (lane == 0) {
-            subsum[j] = sj;
-            submax[j] = wm;
-        }
-    };
-
-    for (int j0 = warp; j0 < nfull; j0 += kWarps * U) {
-        uint4 za[U], zb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * kWarps;
-            if (j < nfull) fetch<DT>(row, j * kSub + lane * 8, za[u], zb[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * kWarps;
-            if (j < nfull) {
-                float x[8];
-                shifted8<DT>(za[u], zb[u], 0.f, x);
-                tile(j, x);
-            }
+        for (int u = 0; u < kUnroll; ++u) {
+            const int e0 = (int)head + (i + u * kGroup) * kEpv;
+            if (DT == 1)
+                proc_bf16<ROW_SAMPLE>(a, w[u], e0, k);
+            else
+                proc_f32<ROW_SAMPLE>(a, w[u], e0, k);
         }
     }
-    for (int j = nfull + warp; j < nsub; j += kWarps) {
-        float x[8];
-        shifted8_scalar<DT>(row, j * kSub + lane * 8, V, 0.f, -INFINITY, x);
-        tile(j, x);
+    for (; i < v1; i += kGroup) {
+        const uint4 w = ldg_stream(vb + i);
+        const int e0 = (int)head + i * kEpv;
+        if (DT == 1)
+            proc_bf16<ROW_SAMPLE>(a, w, e0, k);
+        else
+            proc_f32<ROW_SAMPLE>(a, w, e0, k);
     }
-    const bool wnan = __any_sync(full, nan);
-    if (lane == 0) sm.wflag[warp] = wnan;
+    if (g == kLazyChunks - 1 && tail0 + gt < V) {
+        const int idx = (int)(tail0 + gt);
+        proc_scalar<ROW_SAMPLE>(a, load_elem<DT>(row, idx), idx, k);
+    }
+    Part p{a.m, a.s0 + a.s1, a.arg, a.flags};
+    p = warp_merge<ROW_SAMPLE>(p, k);
+    if (lane == 0) sm.part[warp] = p;
     __syncthreads();
     if (warp == 0) {
-        float M = -INFINITY;
-        for (int j = lane; j < nsub; j += 32) M = fmaxf(M, submax[j]);
+        p = lane < kWarps ? sm.part[lane] : Part{-INFINITY, 0.f, kNone, 0};
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(full, M, o));
-        KSum acc;
-        for (int j = lane; j < nsub; j += 32) {
-            const float mj = submax[j];
-            const float r = (mj == -INFINITY || M == INFINITY) ? 0.f : subsum[j] * ex2((mj - M) * k);
-            subsum[j] = r;
-            acc.add(r);
-        }
-        double S = acc.value();
+        for (int o = 1; o < kWpg; o <<= 1) p = merge<ROW_SAMPLE>(p, shfl_part(p, o), k);
+        if (lane < kWarps && lane % kWpg == 0) sm.cpart[lane / kWpg] = make_float2(p.m, p.s);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(full, S, o);
-        int flags = (lane < kWarps && sm.wflag[lane]) ? rowpass::F_NAN : 0;
-        flags = __reduce_or_sync(full, flags);
-        if (M == INFINITY) flags |= rowpass::F_POSINF;
-        if (M == -INFINITY) flags |= rowpass::F_ALLNEG;
-        if (lane == 0) sm.part_out = rowpass::Part{M, (float)S, 0, flags};
+        for (int o = kWpg; o < 32; o <<= 1) p = merge<ROW_SAMPLE>(p, shfl_part(p, o), k);
+        if (p.m == INFINITY) p.flags |= F_POSINF;
+        if (p.m == -INFINITY) p.flags |= F_ALLNEG;
+        if (lane == 0) sm.part_out = p;
     }
     __syncthreads();
 }
@@ -658,8 +651,7 @@ __device__ void lazy_row_pass(const char *row, int V, float k, Smem &sm, float *
 // node, of its draft row) with the same per-element arithmetic as the row-statistics
 // kernel, plus e_t at the children's tokens. All threads call it; it ends synchronised.
 template <int DT, int DK, int DDT>
-__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd,
-                           float *subsum, float *submax) {
+__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
     constexpr int kDEsz = kDDT == 1 ? 2 : 4;
@@ -684,9 +676,9 @@ __device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int
         const bool kids = __any_sync(0xffffffffu, any);
         if (lane == 0) sm.haskids = kids;
     }
-    lazy_row_pass<DT>(zrow, (int)V, k, sm, subsum, submax);
+    lazy_row_pass<DT>(zrow, V, k, sm);
     const rowpass::Part p = sm.part_out;
-    if (threadIdx.x == 0) sm.subsum_node = nd;
+    if (threadIdx.x == 0) sm.cpart_node = nd;
     if (warp == 0) {
         const float negm = p.m == -INFINITY ? 0.f : -p.m;
 #pragma unroll
@@ -754,8 +746,7 @@ template <int DT, int DK, int DDT, bool LAZY>
 __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     walk_sample_kernel(SampleWalkParams P) {
     __shared__ Smem sm;
-    extern __shared__ float subsum[];   // sub-tile sums; lazy walks add the sub-tile maxima
-    float *submax = subsum + (P.V + kSub - 1) / kSub;
+    extern __shared__ float subsum[];   // sub-tile sums of the current pass
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
@@ -793,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         sm.nlev = 0;
         sm.pending = 0;
         sm.bonus = -1;
-        sm.subsum_node = -1;
+        sm.cpart_node = -1;
     }
     __syncthreads();
 
@@ -845,10 +836,9 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         cmd = sm.cmd;
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
         if (LAZY && cmd == CMD_STATS) {
-            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node, subsum, submax);
+            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node);
             continue;
         }
-        if (tid == 0) sm.subsum_node = -1;   // the pass overwrites the stored sums
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
         residual_pass<DT, DK, DDT>(c, sm, subsum);
     }
@@ -856,19 +846,22 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     if (cmd == CMD_BONUS) {
         const float ub = sm.u[N];
         bool drawn = false;
-        if (!LAZY && DK == DRAFT_POINT && P.chunk != nullptr) {
-            // One chunk instead of the row: locate the chunk from the row-statistics partials,
-            // then sum and search only its sub-tiles. Rows that are not 16-byte aligned have
-            // no partials.
+        if (DK == DRAFT_POINT) {
+            // One chunk instead of the row: locate the chunk from the chunk partials of the
+            // stop row (the row-statistics kernel's, or those of the lazy pass over it), then
+            // sum and search only its sub-tiles. Rows that are not 16-byte aligned have no
+            // partials.
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
-            if (c.zvec) {
-                if (warp == 0)
-                    chunk_pick(c, sm, P.chunk + (base + sm.node) * kRowChunks, ub);
+            constexpr int nc = LAZY ? kLazyChunks : kRowChunks;
+            const float2 *part =
+                LAZY ? (sm.cpart_node == sm.node ? sm.cpart : nullptr)
+                     : (P.chunk ? P.chunk + (base + sm.node) * kRowChunks : nullptr);
+            if (part && c.zvec) {
+                if (warp == 0) chunk_pick(c, sm, part, nc, ub);
                 __syncthreads();
                 const int q = sm.cpick;
                 if (q >= 0) {
-                    const int jlo = row_chunk_sub(q, c.V), jhi = row_chunk_sub(q + 1, c.V);
-                    if (tid == 0) sm.subsum_node = -1;
+                    const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
                     residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
                     if (warp == 0) {
                         const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
@@ -879,22 +872,6 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
                     drawn = sm.bonus >= 0;
                 }
             }
-        }
-        if (LAZY && DK == DRAFT_POINT && sm.subsum_node == sm.node) {
-            // Single pass: the stored sub-tile sums of this row minus the rejected tokens.
-            if (tid == 0)
-                for (int i = 0; i < sm.nR; ++i) {
-                    const int j = sm.R[i] / kSub;
-                    subsum[j] = fmaxf(subsum[j] - sm.RE[i], 0.f);
-                }
-            __syncthreads();
-            const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
-            if (warp == 0) {
-                const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub);
-                if (lane == 0) sm.bonus = v;
-            }
-            __syncthreads();
-            drawn = sm.bonus >= 0;
         }
         for (int attempt = 0; attempt < 3 && !drawn; ++attempt) {
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
@@ -950,19 +927,11 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
-    const size_t nsub = (size_t)((p.V + kSub - 1) / kSub);
-    if (p.lazy) {
-        const size_t smem = 2 * sizeof(float) * nsub;   // sub-tile sums and maxima
-        if (smem > 48 * 1024) {
-            const cudaError_t e = cudaFuncSetAttribute(walk_sample_kernel<DT, DK, DDT, true>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+    const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);   // sub-tile sums
+    if (p.lazy)
         walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
-    } else {
-        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, sizeof(float) * nsub, st>>>(p);
-    }
+    else
+        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -53,7 +53,8 @@ def oracle_budgeted(orc, x, n_active, mode, T=None, kind=G.SPEC_DRAFT_POINT):
     tok, par = x["draft_token"].cpu().numpy(), x["parent"].cpu().numpy()
     u = x["uniforms"].cpu().numpy()
     B, N = par.shape
-    res = {k: [] for k in KEYS + ("decision_margin", "cdf_margin", "cdf_alt")}
+    res = {k: [] for k in KEYS + ("decision_margin", "cdf_margin", "cdf_alt", "cdf_lo",
+                                  "cdf_hi")}
     for b in range(B):
         lg, tk, pr, uu, dr = BU.truncate(logits[b], tok[b], par[b], u[b], int(n_active[b]),
                                          None if draft is None else draft[b])

@@ -202,15 +202,43 @@ def test_sample_rejected_mass_resummed(h, orc):
     """The first child holds almost all the mass and is rejected: the next sibling's
     denominator is re-summed over the row."""
     B, N, V = 8, 4, 151936
-    logits = (3.0 * torch.randn((B, N, V), device=DEV)).to(torch.bfloat16)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(17)
+    logits = (3.0 * torch.randn((B, N, V), device=DEV, generator=g)).to(torch.bfloat16)
     parent = np.tile(np.array([-1, 0, 0, 0], np.int32), (B, 1))
     tok = np.tile(np.array([0, 11, 22, 33], np.int32), (B, 1))
     logits[:, 0, 11] = 20.0
     logits[:, 0, 22] = 3.0
-    u = torch.rand((B, N + 1), device=DEV)
+    u = torch.rand((B, N + 1), device=DEV, generator=g)
     u[:, 1] = 0.99999
     gpu = PY.gpu_sample(h, logits, _to(tok), _to(parent), 1.0, u)
     ref = PY.oracle_sample(orc, logits, _to(tok), _to(parent), 1.0, u)
+    PY.compare_sample(gpu, ref)
+
+
+@pytest.mark.parametrize("lazy", [False, True])
+@pytest.mark.parametrize("top", [20.0, 16.5, 15.0, 12.0])
+def test_bonus_after_a_heavy_rejection(h, orc, lazy, top):
+    """The root's only child holds a large share of the row's mass (about 97%, 50%, 20% and 1%
+    for these logits against N(0, 3) noise over 151936 tokens) and is rejected: the bonus is
+    drawn from the residual without that token, whose mass is comparable to the rounding of
+    the row sum when the share is large."""
+    B, N, V = 64, 2, 151936
+    g = torch.Generator(device=DEV)
+    g.manual_seed(int(top * 10))
+    logits = (3.0 * torch.randn((B, N, V), device=DEV, generator=g)).to(torch.bfloat16)
+    tok = torch.randint(0, V, (B,), device=DEV, generator=g, dtype=torch.int32)
+    logits[torch.arange(B, device=DEV), 0, tok.long()] = top
+    draft_token = torch.stack([torch.zeros_like(tok), tok], dim=1).contiguous()
+    parent = _to(np.tile(np.array([-1, 0], np.int32), (B, 1)))
+    u = torch.rand((B, N + 1), device=DEV, generator=g)
+    u[:, 1] = 0.999999
+    fn = G.verify_sample_lazy if lazy else G.verify_sample
+    out = fn(h, logits, draft_token, parent, 1.0, u)
+    torch.cuda.synchronize()
+    gpu = PY.to_np(out)
+    ref = PY.oracle_sample(orc, logits, draft_token, parent, 1.0, u)
+    assert (ref["accept_len"] == 0).all()
     PY.compare_sample(gpu, ref)
 
 

@@ -263,3 +263,32 @@ def test_cdf_alt_is_the_token_across_the_nearer_boundary(orc):
     assert r["bonus"].tolist() == [2, 2, 2]
     assert r["cdf_alt"][:2].tolist() == [1, 3]
     assert (r["cdf_margin"][:2] < 1e-6).all() and r["cdf_margin"][2] > 1e-2
+
+
+def test_cdf_window_spans_tokens_within_the_tolerance(orc):
+    """The draw window: tokens with mass whose CDF interval comes within 1e-6 * S of tau.
+    r = (0.5, 1e-9, 2e-9, 0.5 - 3e-9), S = 1: tau = 0.5 + 5e-10 lies inside token 1's
+    interval [0.5, 0.5 + 1e-9), and every interval touches (tau - 1e-6, tau + 1e-6), so the
+    window is tokens 0..3; tau = 0.25 is deep inside token 0 (window 0..0); with a zero-mass
+    token between two halves, tau = 0.5 - 1e-7 gives 0..2 (token 1 has no mass but lies
+    inside, tokens 0 and 2 are the ends)."""
+    v, m, win = orc.inv_cdf(np.array([0.5, 1e-9, 2e-9, 0.5 - 3e-9]), 0.5 + 5e-10, window=True)
+    assert v == 1 and m < 1e-9 and win == (0, 3)
+    v, m, win = orc.inv_cdf(np.array([0.5, 1e-9, 2e-9, 0.5 - 3e-9]), 0.25, window=True)
+    assert v == 0 and win == (0, 0)
+    v, m, win = orc.inv_cdf(np.array([0.5, 0.0, 0.5]), 0.5 - 1e-7, window=True)
+    assert v == 0 and win == (0, 2)
+    v, m, win = orc.inv_cdf(np.array([0.25, 0.25, 0.25, 0.25]), 0.6, window=True)
+    assert v == 2 and win == (2, 2)
+    # brute force on random rows: the window is exactly the tokens with mass whose interval
+    # meets [tau - 1e-6 S, tau + 1e-6 S)
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        r = rng.random(12) ** 8 * (rng.random(12) < 0.8)
+        u = rng.random()
+        v, m, win = orc.inv_cdf(r, u, window=True)
+        S = r.sum()
+        C = np.cumsum(r)
+        lo, hi = u * S - 1e-6 * S, u * S + 1e-6 * S
+        want = [w for w in range(12) if r[w] > 0 and C[w] > lo and C[w] - r[w] < hi]
+        assert win == (min(want + [v]), max(want + [v])), (r, u, win, want)

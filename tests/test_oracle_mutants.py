@@ -3,7 +3,8 @@
 Each case copies ``oracle/oracle.c``, plants one plausible mistake by text substitution (a
 wrong comparison, a dropped term, a wrong index, a swapped operand), compiles the copy and runs
 a battery built from the same pins as the other oracle tests: the hand-worked goldens, exact
-and Monte-Carlo losslessness, the two-token closed form and the graph-ancestor mask check. The
+and Monte-Carlo losslessness, the two-token closed form, a hand-worked inverse-CDF draw window
+and the graph-ancestor mask check. The
 battery must fail for every mutant and pass for the unmodified source.
 """
 import itertools
@@ -34,11 +35,14 @@ MUTANTS = {
     "dense_accept_against_p": ("if (lhs < r[x]) {", "if (lhs < p[x]) {"),
     "temperature_dropped": ("p[v] = exp((elem(row, dtype, v) - m) / T);",
                             "p[v] = exp((elem(row, dtype, v) - m));"),
-    "bonus_uniform_slot": ("inv_cdf(r, V, (double)u[N], &cm, &alt);\n    *cmargin = cm;\n    *calt = (int32_t)alt;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row",
-                           "inv_cdf(r, V, (double)u[N - 1], &cm, &alt);\n    *cmargin = cm;\n    *calt = (int32_t)alt;\n    *L_out = L;\n    return (int32_t)bonus;\n}\n\n/* Draft row"),
+    "bonus_uniform_slot": ("for (int64_t v = 0; v < V; v++) r[v] = inR[v] ? 0.0 : p[v];\n    double cm;\n    int64_t alt, win[2];\n    int64_t bonus = inv_cdf(r, V, (double)u[N], &cm, &alt, win);",
+                           "for (int64_t v = 0; v < V; v++) r[v] = inR[v] ? 0.0 : p[v];\n    double cm;\n    int64_t alt, win[2];\n    int64_t bonus = inv_cdf(r, V, (double)u[N - 1], &cm, &alt, win);"),
     "draft_row_of_child": ("draft_row(draft, draft_kind, draft_dtype, grow, V, T, q)",
                            "draft_row(draft, draft_kind, draft_dtype, grow + 1, V, T, q)"),
     "greedy_ignores_token": ("if (par[c] == node && tok[c] == a) {", "if (par[c] == node) {"),
+    "window_low_end_at_tau": ("if (win[0] < 0 && C > tau - delta) win[0] = v;",
+                              "if (win[0] < 0 && C > tau) win[0] = v;"),
+    "window_high_end_at_tau": ("if (Cprev >= tau + delta) break;", "if (Cprev >= tau) break;"),
 }
 
 
@@ -99,6 +103,10 @@ def _battery(orc) -> list:
                               np.array([[0.0, u1, 0.3]], np.float32))
         if r["accept_len"][0] != want:
             failed.append("closed-form")
+    # the draw window of a hand-worked inverse CDF (tokens 1 and 2 have tiny mass)
+    _, _, win = orc.inv_cdf(np.array([0.5, 1e-9, 2e-9, 0.5 - 3e-9]), 0.5 + 5e-10, window=True)
+    if win != (0, 3):
+        failed.append("window")
     # mask against graph ancestors
     par = np.array([[-1, 0, 0, 1, 3, 2, 5, 5]], np.int32)
     anc, depth, _ = orc.build_mask(par)
