@@ -38,6 +38,10 @@
 namespace specv {
 namespace {
 
+#ifndef SPEC_LAZY_UNROLL
+#define SPEC_LAZY_UNROLL 6   // 16-byte loads in flight per thread in the lazy row pass
+#endif
+
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSub = kSubTile;   // elements per sub-tile: 32 lanes x 8
@@ -585,7 +589,7 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
     constexpr int kGroup = kThreads / kLazyChunks;   // threads per chunk
     constexpr int kWpg = kWarps / kLazyChunks;       // warps per chunk
     static_assert(kWpg >= 1 && kLazyChunks <= 32, "lazy chunks");
-    constexpr int kUnroll = 4;
+    constexpr int kUnroll = SPEC_LAZY_UNROLL;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     Acc a;
     a.m = -INFINITY;
