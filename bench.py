@@ -255,18 +255,28 @@ def bench_ours(args):
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
-        G.spec_profile_begin(h)
-        torch.cuda.synchronize(dev)
         start.record(stream)
         for _ in range(args.steps):
             step()
         end.record(stream)
         torch.cuda.synchronize(dev)
-        prof = G.spec_profile_end(h)
     barrier(world)
     ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, world, dev)
     value = aggregate_throughput(world, w.draft_nodes, ms)
+    # Per-kernel durations: the same K steps again with CUDA events around every launch (on the
+    # launching stream). The events sit between the kernels, so they also stop the stages from
+    # overlapping their launches; that is why the headline region above runs without them.
+    G.spec_profile_begin(h)
+    torch.cuda.synchronize(dev)
+    ps, pe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ps.record(stream)
+    for _ in range(args.steps):
+        step()
+    pe.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = G.spec_profile_end(h)
+    ms_profiled = max_over_ranks(ps.elapsed_time(pe) / args.steps, world, dev)
 
     # dominant kernel: row statistics over all B*N rows
     rs_ms, rs_n = prof["row_stats"]
@@ -442,6 +452,7 @@ def bench_ours(args):
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
                 "lazy": lazy,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
+                "ms_per_step_with_kernel_events": ms_profiled,
                 "clocks": clocks.summary(), "accept_len_hist": hist}
         print(json.dumps(line), flush=True)
     h.close()

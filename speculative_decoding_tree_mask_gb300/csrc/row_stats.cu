@@ -47,6 +47,8 @@ template <int DT, int MODE>
 __global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(RowStatsParams P) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
+    grid_dep_wait();     // the logits (and the tree) come from earlier kernels
+    grid_dep_launch();   // the walk may start launching: it waits for this grid's results
     const int row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t V = P.V;
@@ -178,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(
 
 template <int DT, int MODE>
 cudaError_t launch(const RowStatsParams &p, cudaStream_t st) {
-    row_stats_kernel<DT, MODE><<<p.rows, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(row_stats_kernel<DT, MODE>, dim3(p.rows), dim3(kThreads), 0, st, p);
 }
 
 }  // namespace

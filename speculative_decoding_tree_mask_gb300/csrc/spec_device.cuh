@@ -60,6 +60,17 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     return v;
 }
 
+// Programmatic dependent launch. A kernel launched with launch_dependent (spec_internal.h)
+// may start while the kernel before it in the stream still runs; grid_dep_wait() returns once
+// that kernel has completed and its writes are visible (at once for an ordinary launch).
+// grid_dep_launch() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Scalar element load as float (bf16 or f32 storage).
 template <int DT>
 __device__ __forceinline__ float load_elem(const void *row, int64_t i);

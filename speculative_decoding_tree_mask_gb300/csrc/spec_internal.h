@@ -8,6 +8,25 @@
 
 namespace specv {
 
+// Launches `kernel` on `st` allowing it to start before the previous kernel in the stream has
+// finished (programmatic dependent launch): the kernel must call grid_dep_wait() before it
+// reads anything an earlier kernel writes. Hides the launch latency between the stages.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)
 
 enum RowMode { ROW_GREEDY = 0, ROW_SAMPLE = 1, ROW_PROBS = 2 };

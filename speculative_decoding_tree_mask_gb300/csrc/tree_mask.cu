@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
                      int32_t *__restrict__ status) {
     __shared__ unsigned long long s_anc[kWarpsPerCta][kMaxN];
     __shared__ int s_hop[kWarpsPerCta][kMaxN];
+    grid_dep_launch();   // a verify call after this one may start launching (it waits for us)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarpsPerCta + warp;
     if (b >= B) return;

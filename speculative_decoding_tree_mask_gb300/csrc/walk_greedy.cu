@@ -19,6 +19,7 @@ constexpr int kGreedyWarps = 4;
 
 __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWalkParams P) {
     const unsigned full = 0xffffffffu;
+    grid_dep_wait();   // row statistics of the kernel before
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kGreedyWarps + warp;
     if (b >= P.B) return;
@@ -119,8 +120,7 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
 cudaError_t launch_walk_greedy(const GreedyWalkParams &p, cudaStream_t st) {
     if (p.B <= 0) return cudaSuccess;
     const int grid = (p.B + kGreedyWarps - 1) / kGreedyWarps;
-    walk_greedy_kernel<<<grid, 32 * kGreedyWarps, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(walk_greedy_kernel, dim3(grid), dim3(32 * kGreedyWarps), 0, st, p);
 }
 
 }  // namespace specv

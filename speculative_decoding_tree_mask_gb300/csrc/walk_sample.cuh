@@ -762,13 +762,15 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         sm.par[tid] = -2;
         sm.tok[tid] = -1;
     }
-    if (tid < nb && LAZY) {
+    if (tid < nb) {
         sm.par[tid] = P.parent[base + tid];
         sm.tok[tid] = P.tok[base + tid];
     }
+    if (tid <= N) sm.u[tid] = P.uniforms[(size_t)b * (N + 1) + tid];
+    // Eager walks are launched to overlap the row-statistics kernel's end: its results are
+    // read only after it has completed (the tree and uniforms above come from before it).
+    if (!LAZY) grid_dep_wait();
     if (tid < nb && !LAZY) {
-        sm.par[tid] = P.parent[base + tid];
-        sm.tok[tid] = P.tok[base + tid];
         sm.flags[tid] = P.flags[base + tid];
         sm.s[tid] = P.s[base + tid];
         sm.m[tid] = P.m[base + tid];
@@ -782,7 +784,6 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             }
         }
     }
-    if (tid <= N) sm.u[tid] = P.uniforms[(size_t)b * (N + 1) + tid];
     if (tid == 0) {
         sm.nR = 0;
         sm.nlev = 0;
@@ -932,10 +933,10 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
     const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);   // sub-tile sums
-    if (p.lazy)
-        walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
-    else
-        walk_sample_kernel<DT, DK, DDT, false><<<p.B, kThreads, smem, st>>>(p);
+    if (!p.lazy)
+        return launch_dependent(walk_sample_kernel<DT, DK, DDT, false>, dim3(p.B),
+                                dim3(kThreads), smem, st, p);
+    walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
