@@ -425,3 +425,26 @@ def test_side_stream_and_profiling(h):
     assert prof["row_stats"][0] > 0
     for k in PY.KEYS:
         assert np.array_equal(out[k].cpu().numpy(), ref[k])
+
+
+def test_verify_waits_for_the_kernel_that_writes_the_logits(h, orc):
+    """The stages are launched as programmatic dependents; each must still see everything the
+    kernels before it in the stream wrote. Two inputs whose greedy results differ are copied
+    alternately into one buffer by a device copy kernel, each copy followed at once (no
+    synchronisation) by a verify call on the same stream."""
+    w = W.WORKLOADS["greedy_trie"].scaled(B=16, V=40000)
+    xa, xb = W.make(w, device=DEV, seed=31), W.make(w, device=DEV, seed=32)
+    xb["draft_token"] = xa["draft_token"]
+    xb["parent"] = xa["parent"]
+    ref = {k: orc.verify_greedy(PY.host(x["logits"]), xa["tok_np"], xa["parent_np"])
+           for k, x in (("a", xa), ("b", xb))}
+    assert not np.array_equal(ref["a"]["bonus"], ref["b"]["bonus"])
+    buf = torch.empty_like(xa["logits"])
+    outs = []
+    for i in range(12):
+        buf.copy_((xa if i % 2 == 0 else xb)["logits"])
+        o = G.verify_greedy(h, buf, xa["draft_token"], xa["parent"])
+        outs.append({k: v.clone() for k, v in o.items()})
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        PY.assert_exact(PY.to_np(o), ref["a" if i % 2 == 0 else "b"])
