@@ -68,6 +68,7 @@ struct Smem {
     double ctau;                       // ... and tau relative to the chunk's start
     int cpart_node;                    // lazy: node whose chunk partials are in cpart[]
     float2 cpart[kLazyChunks];         // lazy: (max, sum) of each chunk of that node's row
+    float2 epart[kMaxN][kRowChunks];   // eager point drafts: chunk partials of every node's row
     int wflag[kWarps];
     rowpass::Part part[kWarps], part_out;
 };
@@ -210,11 +211,11 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
 // ---- one pass over the node's residual ----------------------------------------------------
 
 // Every warp sums its sub-tiles of [jlo, jhi) (default: the whole row) into subsum[] (one warp
-// scan per 256 elements); the total lands in sm.total. All threads call it; it ends
-// synchronised.
+// scan per 256 elements); with `total`, their sum lands in sm.total. All threads call it; it
+// ends synchronised.
 template <int DT, int DK, int DDT>
 __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0,
-                              int jhi = INT_MAX) {
+                              int jhi = INT_MAX, bool total = true) {
     // sub-tiles in flight per warp (32 registers of raw loads)
     constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : 2;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
@@ -265,6 +266,10 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
         }
     }
 
+    if (!total) {
+        __syncthreads();
+        return;
+    }
     if (lane == 31) sm.wtot[warp] = wsum.value();
     __syncthreads();
     if (warp == 0) {
@@ -413,14 +418,14 @@ __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, f
     }
     const double incl = warp_incl_scan_d(M);
     const double S = __shfl_sync(full, incl, 31);
-    double Ptot = P;
+    float Ptot = (float)P;   // only compared with S / 2
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ptot += __shfl_xor_sync(full, Ptot, o);
     double excl = __shfl_up_sync(full, incl, 1);
     if (lane == 0) excl = 0.0;
     int pick = -1;
     double tau = 0.0;
-    if (S > 0.0 && S >= 0.5 * Ptot) {
+    if (S > 0.0 && S >= 0.5 * (double)Ptot) {
         tau = (double)u * S;
         const unsigned hit = __ballot_sync(full, lane < nc && incl > tau);
         const unsigned pos = __ballot_sync(full, lane < nc && M > 0.0);
@@ -770,6 +775,8 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     // Eager walks are launched to overlap the row-statistics kernel's end: its results are
     // read only after it has completed (the tree and uniforms above come from before it).
     if (!LAZY) grid_dep_wait();
+    if (!LAZY && DK == DRAFT_POINT && P.chunk && tid < nb * kRowChunks)
+        (&sm.epart[0][0])[tid] = P.chunk[base * kRowChunks + tid];
     if (tid < nb && !LAZY) {
         sm.flags[tid] = P.flags[base + tid];
         sm.s[tid] = P.s[base + tid];
@@ -858,16 +865,15 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             // partials.
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
             constexpr int nc = LAZY ? kLazyChunks : kRowChunks;
-            const float2 *part =
-                LAZY ? (sm.cpart_node == sm.node ? sm.cpart : nullptr)
-                     : (P.chunk ? P.chunk + (base + sm.node) * kRowChunks : nullptr);
+            const float2 *part = LAZY ? (sm.cpart_node == sm.node ? sm.cpart : nullptr)
+                                      : (P.chunk ? sm.epart[sm.node] : nullptr);
             if (part && c.zvec) {
                 if (warp == 0) chunk_pick(c, sm, part, nc, ub);
                 __syncthreads();
                 const int q = sm.cpick;
                 if (q >= 0) {
                     const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                    residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
+                    residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);
                     if (warp == 0) {
                         const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
                                                                 sm.ctau);
