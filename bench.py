@@ -292,6 +292,33 @@ def bench_ours(args):
     kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
                for k, v in prof.items() if v[1]}
 
+    # greedy verification of the same trees (argmax path, no exponentials)
+    gout = G.alloc_outputs(B, N, dev)
+
+    def greedy_step():
+        G.spec_build_tree_mask(h, x["parent"], mask["anc_mask"], mask["depth"], mask["status"],
+                               stream)
+        G.spec_verify_greedy(h, x["logits"], x["draft_token"], x["parent"], gout["accept_len"],
+                             gout["out_tokens"], gout["kv_commit"], gout["bonus"],
+                             gout["status"], stream=stream)
+
+    for _ in range(args.warmup):
+        greedy_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gs.record(stream)
+    for _ in range(args.steps):
+        greedy_step()
+    ge.record(stream)
+    torch.cuda.synchronize(dev)
+    gms = max_over_ranks(gs.elapsed_time(ge) / args.steps, world, dev)
+    greedy = {"value": aggregate_throughput(world, w.draft_nodes, gms), "unit": UNIT,
+              "ms_per_step": gms, "logit_GBps": alg_bytes / (gms / 1e3) / 1e9,
+              "path": "tree mask + spec_verify_greedy (row statistics without exponentials, "
+                      "warp-per-request walk)",
+              "accept_len_mean": float(gout["accept_len"].float().mean().item())}
+
     # lazy verification: the same outputs, reading only the rows the walk visits
     lazy = None
     if not args.skip_lazy:
@@ -450,7 +477,7 @@ def bench_ours(args):
                 "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
                 "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
-                "lazy": lazy,
+                "greedy": greedy, "lazy": lazy,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
                 "ms_per_step_with_kernel_events": ms_profiled,
                 "clocks": clocks.summary(), "accept_len_hist": hist}

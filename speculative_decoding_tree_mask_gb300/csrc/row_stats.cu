@@ -90,12 +90,7 @@ __global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(
     }
 
     const float k = P.k;
-    Acc a;
-    a.m = -INFINITY;
-    a.negm = 0.f;
-    a.s0 = a.s1 = 0.f;
-    a.arg = kNone;
-    a.flags = 0;
+    Acc a = acc_init();
 
     // Split the row into a scalar head up to 16-byte alignment, vectors, and a scalar tail;
     // thread group g takes vectors [row_chunk_vec(g), row_chunk_vec(g + 1)), group 0 the head

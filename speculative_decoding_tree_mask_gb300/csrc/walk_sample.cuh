@@ -596,12 +596,7 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
     static_assert(kWpg >= 1 && kLazyChunks <= 32, "lazy chunks");
     constexpr int kUnroll = SPEC_LAZY_UNROLL;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    Acc a;
-    a.m = -INFINITY;
-    a.negm = 0.f;
-    a.s0 = a.s1 = 0.f;
-    a.arg = kNone;
-    a.flags = 0;
+    Acc a = acc_init();
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
     int64_t head = (int64_t)((16 - (addr & 15)) & 15) / kEsz;
     if (head > V) head = V;
