@@ -19,10 +19,15 @@
 //     normalises the next residual level;
 //   * bonus: the residual at the stop node is summed per 256-element sub-tile (a warp scan
 //     over 32 lanes x 8 elements), the sub-tile sums stay in shared memory, warp 0 locates
-//     the sub-tile holding tau = u * S (scan of per-lane chunk sums, then of the chosen
-//     chunk) and re-reads only that sub-tile to find the token.
+//     the sub-tile holding tau = u * S (scan of per-lane groups of sub-tile sums, then of the
+//     chosen group) and re-reads only that sub-tile to find the token. With point drafts the
+//     pass covers one chunk of the row only: the row-statistics kernel (eager) or the lazy
+//     pass leaves the (max, sum) of every chunk of the row, from which warp 0 first picks the
+//     chunk holding tau (the rejected tokens' mass taken out of their chunks).
 // Every search level falls back to the last token with r(v) > 0 when rounding leaves tau past
 // its end, so the drawn token always has positive residual mass.
+// Lazy walks (no row-statistics kernel) stream each row they visit when they enter it, one
+// chunk per warp with the row-statistics kernel's per-element code.
 // A pass issues the 16-byte loads of 8 sub-tiles per lane before using any of them (2 CTAs
 // per SM: 128 KiB of each SM's loads in flight); sums use compensated float32, and the
 // float64 pipe (slow on this part) only sees a handful of operations per decision.
