@@ -459,6 +459,10 @@ def bench_ours(args):
                     "h2d_GBps": (hl.numel() * hl.element_size() + small_h2d) / cms / 1e6,
                     "path": "all logits copied host to device, then spec_verify_sample"}
 
+    # f2 and f1 on their own workloads: the KV commit after a verify call, and the dense chain
+    extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
+                                        "dense_chain": bench_dense_chain(dev, stream, args)}
+
     cpu = None
     if rank == 0 and not args.skip_cpu_baseline:
         nthreads = os.cpu_count() or 1
@@ -477,7 +481,7 @@ def bench_ours(args):
                 "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
                 "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
-                "greedy": greedy, "lazy": lazy,
+                "greedy": greedy, "lazy": lazy, **extra,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
                 "ms_per_step_with_kernel_events": ms_profiled,
                 "clocks": clocks.summary(), "accept_len_hist": hist}
@@ -485,6 +489,89 @@ def bench_ours(args):
     h.close()
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _time_calls(fn, stream, steps, warmup, flush=None):
+    """Mean device milliseconds of fn() over `steps` calls (events on `stream`), each call
+    preceded by an L2 flush when `flush` (a device buffer larger than L2) is given: the buffer
+    is read, so the flush leaves no dirty lines to be written back during the timed call."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        if flush is not None:
+            flush.max()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        total += a.elapsed_time(z)
+    return total / steps
+
+
+def bench_kv_commit(h, dev, stream, args):
+    """KV commit of 8 slots per request (root + 7 accepted) for B=256, N=64, 32 heads x 128,
+    bf16 sources, into an NHD paged cache of 16-token blocks: bf16 and fp8 (e4m3) caches."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    B, N, H, D, bs = 256, 64, 32, 128, 16
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    src_k = torch.randn((B, N, H, D), device=dev, generator=g).to(torch.bfloat16)
+    src_v = torch.randn((B, N, H, D), device=dev, generator=g).to(torch.bfloat16)
+    L = 7
+    kv = torch.full((B, N), -1, dtype=torch.int32, device=dev)
+    kv[:, :L + 1] = torch.arange(L + 1, dtype=torch.int32, device=dev) * 5   # root, then a path
+    kv[:, 0] = 0
+    al = torch.full((B,), L, dtype=torch.int32, device=dev)
+    max_blocks = 8
+    table = torch.randperm(B * max_blocks, device=dev, generator=g).to(torch.int32).view(
+        B, max_blocks)
+    pos = torch.full((B,), 37, dtype=torch.int32, device=dev)
+    flush = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, cache_kind, esz in (("bf16", G.SPEC_CACHE_SAME, 2), ("fp8_e4m3",
+                                                                   G.SPEC_CACHE_FP8_E4M3, 1)):
+        cdt = torch.bfloat16 if esz == 2 else torch.uint8
+        ck = torch.zeros((B * max_blocks, bs, H, D), dtype=cdt, device=dev)
+        cv = torch.zeros_like(ck)
+        scale = torch.tensor([0.5], device=dev) if esz == 1 else None
+
+        def call():
+            G.spec_kv_commit(h, src_k, src_v, kv, al, ck, cv, G.SPEC_KV_NHD, table, pos,
+                             cache_kind=cache_kind, k_scale=scale, v_scale=scale, stream=stream)
+
+        ms = _time_calls(call, stream, 50, 5, flush)
+        moved = B * (L + 1) * 2 * H * D * (2 + esz)   # read K and V, write them into the cache
+        out[name] = {"ms_per_call": ms, "bytes": moved, "GBps": moved / (ms / 1e3) / 1e9}
+    out["config"] = ("B=256 N=64, 8 slots per request, H=32 D=128 bf16 sources, NHD cache of "
+                     "16-token blocks; L2 flushed before every call")
+    return out
+
+
+def bench_dense_chain(dev, stream, args):
+    """The dense-chain workload (B=64, k=5, V=128256, bf16 target and draft logits), one
+    spec_verify_sample call with dense draft logits; L2 flushed before every call."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    w = W.WORKLOADS["dense_chain"]
+    x = W.make(w, device=dev, seed=w.seed)
+    with G.Handle(w.B, w.N, w.V, dev.index if dev.index is not None else 0) as hd:
+        out = G.alloc_outputs(w.B, w.N, dev)
+        flush = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+        def call():
+            G.verify_sample(hd, x["logits"], x["draft_token"], x["parent"], w.temperature,
+                            x["uniforms"], draft=x["draft"], draft_kind=G.SPEC_DRAFT_LOGITS,
+                            out=out, stream=stream)
+
+        ms = _time_calls(call, stream, 50, 5, flush)
+        moved = 2 * x["logits"].numel() * x["logits"].element_size()
+        return {"ms_per_call": ms, "value": w.B * (w.N - 1) / (ms / 1e3), "unit": UNIT,
+                "logits_bytes": moved,
+                "accept_len_mean": float(out["accept_len"].float().mean().item()),
+                "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft logits, "
+                          "T=1; L2 flushed before every call"}
 
 
 def main(argv=None):
@@ -496,6 +583,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="leave out the KV-commit and dense-chain measurements")
     ap.add_argument("--skip-lazy", action="store_true")
     ap.add_argument("--requests", type=int, default=0,
                     help="requests per rank (default: the workload's 256); for profiling runs")
