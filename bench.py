@@ -461,7 +461,9 @@ def bench_ours(args):
 
     # f2 and f1 on their own workloads: the KV commit after a verify call, and the dense chain
     extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
-                                        "dense_chain": bench_dense_chain(dev, stream, args)}
+                                        "dense_chain": bench_dense_chain(dev, stream, args),
+                                        "adaptive_budget": bench_budget(h, x, w, dev, stream,
+                                                                        args)}
 
     cpu = None
     if rank == 0 and not args.skip_cpu_baseline:
@@ -572,6 +574,63 @@ def bench_dense_chain(dev, stream, args):
                 "accept_len_mean": float(out["accept_len"].float().mean().item()),
                 "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft logits, "
                           "T=1; L2 flushed before every call"}
+
+
+def bench_budget(h, x, w, dev, stream, args):
+    """f4: the large-tree step (mask + eager sampling verify) followed by the device-side budget
+    controller, captured once in a CUDA graph and replayed; the node budget starts at 16 of
+    64 and the controller moves it (target acceptance ratio 0.5). Rows beyond a request's
+    budget are not read."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    B, N, T = w.B, w.N, w.temperature
+    n_active = torch.full((B,), 16, dtype=torch.int32, device=dev)
+    state = G.budget_state(0.5, 16, dev)
+    prm = G.BudgetParams(0.5, 0.25, 0.05, 4, N, 4)
+    mask = dict(anc_mask=torch.empty((B, N), dtype=torch.int64, device=dev),
+                depth=torch.empty((B, N), dtype=torch.int32, device=dev),
+                status=torch.empty(B, dtype=torch.int32, device=dev))
+    out = G.alloc_outputs(B, N, dev)
+    side = torch.cuda.Stream(dev)
+
+    def step():
+        G.spec_build_tree_mask(h, x["parent"], mask["anc_mask"], mask["depth"], mask["status"],
+                               side)
+        G.spec_verify_sample(h, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"],
+                             out["accept_len"], out["out_tokens"], out["kv_commit"],
+                             out["bonus"], out["status"], stream=side)
+        G.spec_budget_update(h, prm, out["accept_len"], out["status"], x["parent"], state,
+                             n_active, stream=side)
+
+    G.spec_set_node_budget(h, n_active)
+    try:
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+            side.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                step()
+        stream.wait_stream(side)
+        state.copy_(G.budget_state(0.5, 16, dev))
+        n_active.fill_(16)
+        torch.cuda.synchronize()
+        budgets = []
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = 200
+        a.record(stream)
+        for i in range(steps):
+            graph.replay()
+        z.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(z) / steps
+        ema, budget, nsteps = G.read_budget_state(state)
+    finally:
+        G.spec_set_node_budget(h, None)
+    return {"ms_per_step": ms, "final_budget": budget, "final_ema": ema, "updates": nsteps,
+            "path": "tree mask + spec_verify_sample under a device node budget + "
+                    "spec_budget_update, one CUDA graph replayed per step",
+            "config": "large tree; budget starts at 16 nodes, target ratio 0.5, alpha 0.25, "
+                      "band 0.05, step 4, limits 4..64"}
 
 
 def main(argv=None):
