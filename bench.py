@@ -384,6 +384,40 @@ def bench_ours(args):
                 "kernels": {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
                             for k, v in lprof.items() if v[1]},
                 "requests_differing_from_eager": ndiff}
+        # lazy greedy: the argmax path only, same trees, one graph per step
+        lgout = G.alloc_outputs(B, N, dev)
+        ggraph = torch.cuda.CUDAGraph()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            lazy_greedy_on = lambda: (  # noqa: E731
+                G.spec_build_tree_mask(h, x["parent"], mask["anc_mask"], mask["depth"],
+                                       mask["status"], side),
+                G.spec_verify_greedy_lazy(h, x["logits"], x["draft_token"], x["parent"],
+                                          lgout["accept_len"], lgout["out_tokens"],
+                                          lgout["kv_commit"], lgout["bonus"], lgout["status"],
+                                          stream=side))
+            lazy_greedy_on()
+            side.synchronize()
+            with torch.cuda.graph(ggraph, stream=side):
+                lazy_greedy_on()
+        stream.wait_stream(side)
+        for _ in range(args.warmup):
+            ggraph.replay()
+        torch.cuda.synchronize(dev)
+        s5, t5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s5.record(stream)
+        for _ in range(args.steps):
+            ggraph.replay()
+        t5.record(stream)
+        torch.cuda.synchronize(dev)
+        gl_ms = max_over_ranks(s5.elapsed_time(t5) / args.steps, world, dev)
+        lazy["greedy"] = {"value": aggregate_throughput(world, w.draft_nodes, gl_ms),
+                          "ms_per_step": gl_ms,
+                          "rows_streamed_per_step":
+                              int(lgout["accept_len"].sum().item()) + B,
+                          "outputs_equal_eager_greedy": bool(
+                              torch.equal(lgout["out_tokens"], gout["out_tokens"]) and
+                              torch.equal(lgout["kv_commit"], gout["kv_commit"]))}
 
     # End to end, inputs in pinned host memory and results read back every step.
     # e2e: the lazy call reads the logits rows it needs straight from pinned host memory over
