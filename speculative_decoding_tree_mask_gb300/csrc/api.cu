@@ -294,10 +294,12 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     rp.pc = h->pc;
     rp.n_active = h->n_active;
     rp.chunk = h->chunk;
-    rc = timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
-    if (rc != SPEC_OK) return rc;
-
-    if (dense) {
+    if (!dense) {
+        rc = timed(h, SPEC_K_ROW_STATS, st,
+                   [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
+        if (rc != SPEC_OK) return rc;
+    } else {
+        // The draft rows of the inner nodes are streamed in the same launch as the target rows.
         RowStatsParams dp = rp;
         dp.x = draft;
         dp.chunk = nullptr;   // partials are kept for the target rows only
@@ -314,7 +316,9 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
             dp.m = nullptr;
             dp.s = nullptr;
         }
-        rc = timed(h, SPEC_K_DRAFT_STATS, st, [&] { return launch_row_stats(dp, ddt, mode, st); });
+        rc = timed(h, SPEC_K_ROW_STATS, st, [&] {
+            return launch_row_stats_pair(rp, dtype, dp, ddt, mode, st);
+        });
         if (rc != SPEC_OK) return rc;
     }
 

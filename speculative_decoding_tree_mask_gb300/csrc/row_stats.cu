@@ -43,13 +43,13 @@ constexpr int kUnroll = SPEC_ROW_UNROLL;
 constexpr int kGroup = kThreads / kRowChunks;        // threads per chunk
 constexpr int kWarpsPerGroup = kWarps / kRowChunks;
 
-template <int DT, int MODE>
-__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(RowStatsParams P) {
+// The statistics of one row (the whole CTA): row blockIdx.x, or blockIdx.x - first for the
+// second set of a paired launch.
+template <int DT, int MODE, bool SECOND>
+__device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
-    grid_dep_wait();     // the logits (and the tree) come from earlier kernels
-    grid_dep_launch();   // the walk may start launching: it waits for this grid's results
-    const int row = blockIdx.x;
+    const int row = SECOND ? (int)blockIdx.x - first : (int)blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t V = P.V;
     const char *rowp = reinterpret_cast<const char *>(P.x) + (size_t)row * (size_t)V * kEsz;
@@ -174,11 +174,52 @@ __global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(
 }
 
 template <int DT, int MODE>
+__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(RowStatsParams P) {
+    grid_dep_wait();     // the logits (and the tree) come from earlier kernels
+    grid_dep_launch();   // the walk may start launching: it waits for this grid's results
+    row_stats_row<DT, MODE, false>(P, 0);
+}
+
+// Target rows and dense-draft rows in one launch (the first A.rows CTAs take the target rows):
+// both sets are streamed at once instead of one launch after the other.
+template <int DT1, int MODE1, int DT2, int MODE2>
+__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS)
+    row_stats_pair_kernel(RowStatsParams A, RowStatsParams B) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if ((int)blockIdx.x < A.rows)
+        row_stats_row<DT1, MODE1, false>(A, 0);
+    else
+        row_stats_row<DT2, MODE2, true>(B, A.rows);
+}
+
+template <int DT1, int DT2, int MODE2>
+cudaError_t launch_pair(const RowStatsParams &a, const RowStatsParams &b, cudaStream_t st) {
+    return launch_dependent(row_stats_pair_kernel<DT1, ROW_SAMPLE, DT2, MODE2>,
+                            dim3(a.rows + b.rows), dim3(kThreads), 0, st, a, b);
+}
+
+template <int DT1>
+cudaError_t launch_pair_d(const RowStatsParams &a, const RowStatsParams &b, int dtype2,
+                          int mode2, cudaStream_t st) {
+    if (mode2 == ROW_PROBS) return launch_pair<DT1, 0, ROW_PROBS>(a, b, st);
+    if (dtype2 == 1) return launch_pair<DT1, 1, ROW_SAMPLE>(a, b, st);
+    return launch_pair<DT1, 0, ROW_SAMPLE>(a, b, st);
+}
+
+template <int DT, int MODE>
 cudaError_t launch(const RowStatsParams &p, cudaStream_t st) {
     return launch_dependent(row_stats_kernel<DT, MODE>, dim3(p.rows), dim3(kThreads), 0, st, p);
 }
 
 }  // namespace
+
+cudaError_t launch_row_stats_pair(const RowStatsParams &target, int dtype, const RowStatsParams &draft,
+                                  int draft_dtype, int draft_mode, cudaStream_t st) {
+    if (target.rows + draft.rows <= 0) return cudaSuccess;
+    if (dtype == 1) return launch_pair_d<1>(target, draft, draft_dtype, draft_mode, st);
+    return launch_pair_d<0>(target, draft, draft_dtype, draft_mode, st);
+}
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st) {
     if (p.rows <= 0) return cudaSuccess;

@@ -84,6 +84,10 @@ struct RowStatsParams {
 };
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);
+// Sampling statistics of the target rows and of the dense-draft rows in one launch.
+cudaError_t launch_row_stats_pair(const RowStatsParams &target, int dtype,
+                                  const RowStatsParams &draft, int draft_dtype, int draft_mode,
+                                  cudaStream_t st);
 
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
                              int32_t *status, cudaStream_t st);
