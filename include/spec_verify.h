@@ -85,7 +85,7 @@ enum { SPEC_ROW_NAN = 1, SPEC_ROW_POSINF = 2, SPEC_ROW_ALL_NEGINF = 4 };
 enum {
     SPEC_K_TREE_MASK = 0,
     SPEC_K_ROW_STATS = 1,       /* target logits rows */
-    SPEC_K_DRAFT_STATS = 2,     /* dense draft rows */
+    SPEC_K_DRAFT_STATS = 2,     /* reserved: dense draft rows now share the ROW_STATS launch */
     SPEC_K_WALK_GREEDY = 3,
     SPEC_K_WALK_SAMPLE = 4,
     SPEC_K_LAZY_GREEDY = 5,
