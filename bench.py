@@ -496,6 +496,7 @@ def bench_ours(args):
     # f2 and f1 on their own workloads: the KV commit after a verify call, and the dense chain
     extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
                                         "dense_chain": bench_dense_chain(dev, stream, args),
+                                        "small_tries": bench_small_tries(dev, stream, args),
                                         "adaptive_budget": bench_budget(h, x, w, dev, stream,
                                                                         args)}
 
@@ -608,6 +609,36 @@ def bench_dense_chain(dev, stream, args):
                 "accept_len_mean": float(out["accept_len"].float().mean().item()),
                 "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft logits, "
                           "T=1; L2 flushed before every call"}
+
+
+def bench_small_tries(dev, stream, args):
+    """The two small trie workloads (greedy: B=4, sampling: B=8; N=32, V=151936, bf16 logits),
+    one verify call each; L2 flushed before every call. Their 128 and 256 rows fill less
+    than one wave of row CTAs, so each row is streamed by 4 or 2 CTAs."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    res = {}
+    for name in ("greedy_trie", "sampling_trie"):
+        w = W.WORKLOADS[name]
+        x = W.make(w, device=dev, seed=w.seed)
+        with G.Handle(w.B, w.N, w.V, dev.index if dev.index is not None else 0) as hs:
+            out = G.alloc_outputs(w.B, w.N, dev)
+            flush = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+            def call():
+                if w.mode == "greedy":
+                    G.verify_greedy(hs, x["logits"], x["draft_token"], x["parent"], out=out,
+                                    stream=stream)
+                else:
+                    G.verify_sample(hs, x["logits"], x["draft_token"], x["parent"],
+                                    w.temperature, x["uniforms"], out=out, stream=stream)
+
+            ms = _time_calls(call, stream, 50, 5, flush)
+            moved = x["logits"].numel() * x["logits"].element_size()
+            res[name] = {"ms_per_call": ms, "value": w.B * (w.N - 1) / (ms / 1e3), "unit": UNIT,
+                         "logits_bytes": moved, "logit_GBps": moved / (ms / 1e3) / 1e9,
+                         "config": f"{name}: B={w.B} N={w.N} V={w.V} bf16, T={w.temperature}, "
+                                   "L2 flushed before every call"}
+    return res
 
 
 def bench_budget(h, x, w, dev, stream, args):

@@ -97,7 +97,7 @@ enum {
 
 /*
  * Create a handle for `device` able to serve calls with B <= max_B, N <= max_N (<= 64) and
- * V <= max_V (<= 2^21). Allocates a device workspace of 100 * max_B * max_N bytes with
+ * V <= max_V (<= 2^21). Allocates a device workspace of 232 * max_B * max_N bytes with
  * cudaMalloc (released by spec_verify_destroy). Returns SPEC_ERR_ARG for out-of-range limits,
  * SPEC_ERR_CUDA if the device cannot be used, SPEC_ERR_WORKSPACE if allocation fails.
  */

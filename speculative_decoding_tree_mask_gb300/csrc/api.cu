@@ -29,6 +29,9 @@ struct spec_ctx {
           *qc = nullptr;
     int32_t *arg = nullptr, *flags = nullptr, *dflags = nullptr;
     float2 *chunk = nullptr;              // row-chunk partials of the target rows
+    RowPart *piece = nullptr;             // small batches: per-piece row statistics
+    int32_t *count = nullptr;             // ... and per-row arrivals (zero between calls)
+    int slots = 0;                        // CTAs of the row-statistics kernel in one wave
     const int32_t *n_active = nullptr;   // node budget set by spec_set_node_budget
     bool prof = false;
     bool ev_ready = false;
@@ -107,6 +110,21 @@ int check_common(spec_handle h, const void *logits, int dtype, int B, int N, int
     return SPEC_OK;
 }
 
+// Small batches: split every row over the most CTAs (8, 4 or 2) that still fit in one wave,
+// so that the row-statistics kernel keeps every SM streaming. Only for row counts the
+// workspace's per-piece arrays can hold.
+void set_split(spec_handle h, RowStatsParams &rp) {
+    rp.split = 1;
+    if ((int64_t)rp.rows > (int64_t)h->max_B * h->max_N) return;
+    rp.piece = h->piece;
+    rp.count = h->count;
+    for (int s = kRowChunks; s > 1; s /= 2)
+        if ((int64_t)rp.rows * s <= h->slots) {
+            rp.split = s;
+            break;
+        }
+}
+
 WalkOutputs outputs(int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
                     int32_t *bonus, int32_t *status) {
     WalkOutputs o;
@@ -131,6 +149,7 @@ int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int6
     rp.arg = h->arg;
     rp.flags = h->flags;
     rp.n_active = h->n_active;
+    set_split(h, rp);
     int rc = timed(h, SPEC_K_ROW_STATS, st,
                    [&] { return launch_row_stats(rp, dtype, ROW_GREEDY, st); });
     if (rc != SPEC_OK) return rc;
@@ -180,7 +199,8 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
     h->max_N = max_N;
     h->max_V = max_V;
     const size_t rows = (size_t)max_B * max_N;
-    const size_t bytes = rows * (9 * 4 + kRowChunks * sizeof(float2));
+    const size_t bytes =
+        rows * (9 * 4 + kRowChunks * sizeof(float2) + kRowChunks * sizeof(RowPart) + 4);
     if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
@@ -193,6 +213,7 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
         return q;
     };
     h->chunk = reinterpret_cast<float2 *>(take(rows * kRowChunks * sizeof(float2)));
+    h->piece = reinterpret_cast<RowPart *>(take(rows * kRowChunks * sizeof(RowPart)));
     h->m = reinterpret_cast<float *>(take(rows * 4));
     h->s = reinterpret_cast<float *>(take(rows * 4));
     h->pc = reinterpret_cast<float *>(take(rows * 4));
@@ -202,6 +223,16 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
     h->arg = reinterpret_cast<int32_t *>(take(rows * 4));
     h->flags = reinterpret_cast<int32_t *>(take(rows * 4));
     h->dflags = reinterpret_cast<int32_t *>(take(rows * 4));
+    h->count = reinterpret_cast<int32_t *>(take(rows * 4));
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaMemset(h->count, 0, rows * 4) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->ws);
+        delete h;
+        return SPEC_ERR_CUDA;
+    }
+    h->slots = 6 * sms;   // the row-statistics kernel keeps 6 CTAs on every SM
     *out = h;
     return SPEC_OK;
 }
@@ -295,6 +326,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     rp.n_active = h->n_active;
     rp.chunk = h->chunk;
     if (!dense) {
+        set_split(h, rp);
         rc = timed(h, SPEC_K_ROW_STATS, st,
                    [&] { return launch_row_stats(rp, dtype, ROW_SAMPLE, st); });
         if (rc != SPEC_OK) return rc;
@@ -558,6 +590,7 @@ int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N
     rp.arg = row_argmax;
     rp.flags = row_flags;
     rp.pc = gather ? child_prob : nullptr;
+    set_split(h, rp);
     const int mode = temperature > 0.f ? ROW_SAMPLE : ROW_GREEDY;
     return timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, mode, st); });
 }

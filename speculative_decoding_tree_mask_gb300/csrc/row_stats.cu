@@ -40,16 +40,18 @@ using namespace rowpass;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = SPEC_ROW_UNROLL;
-constexpr int kGroup = kThreads / kRowChunks;        // threads per chunk
-constexpr int kWarpsPerGroup = kWarps / kRowChunks;
-
-// The statistics of one row (the whole CTA): row blockIdx.x, or blockIdx.x - first for the
-// second set of a paired launch.
-template <int DT, int MODE, bool SECOND>
+// The statistics of one row: row blockIdx.x (blockIdx.x - first for the second set of a
+// paired launch), or, with SPLIT > 1, piece blockIdx.x % SPLIT of row blockIdx.x / SPLIT.
+template <int DT, int MODE, bool SECOND, int SPLIT = 1>
 __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
-    const int row = SECOND ? (int)blockIdx.x - first : (int)blockIdx.x;
+    constexpr int kChunksPerCta = kRowChunks / SPLIT;
+    constexpr int kGroup = kThreads / kChunksPerCta;         // threads per chunk
+    constexpr int kWarpsPerGroup = kWarps / kChunksPerCta;
+    static_assert(kChunksPerCta * SPLIT == kRowChunks && kWarpsPerGroup >= 1, "row split");
+    const int cta = SECOND ? (int)blockIdx.x - first : (int)blockIdx.x;
+    const int row = cta / SPLIT, piece = cta - row * SPLIT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t V = P.V;
     const char *rowp = reinterpret_cast<const char *>(P.x) + (size_t)row * (size_t)V * kEsz;
@@ -101,7 +103,7 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
     const int nv = (int)((V - head) / kEpv);
     const int64_t tail0 = head + (int64_t)nv * kEpv;
     const bool aligned = head == 0;
-    const int g = tid / kGroup, gt = tid - g * kGroup;
+    const int g = piece * kChunksPerCta + tid / kGroup, gt = tid % kGroup;   // chunk, rank
     const int v1 = row_chunk_vec(g + 1, nv, V, aligned, kEpv);
     if (g == 0 && gt < head) proc_scalar<MODE>(a, load_elem<DT>(rowp, gt), gt, k);
 
@@ -144,9 +146,32 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
 #pragma unroll
     for (int o = 1; o < kWarpsPerGroup; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
     if (MODE == ROW_SAMPLE && P.chunk && aligned && lane < kWarps && lane % kWarpsPerGroup == 0)
-        P.chunk[(size_t)row * kRowChunks + lane / kWarpsPerGroup] = make_float2(p.m, p.s);
+        P.chunk[(size_t)row * kRowChunks + piece * kChunksPerCta + lane / kWarpsPerGroup] =
+            make_float2(p.m, p.s);
 #pragma unroll
     for (int o = kWarpsPerGroup; o < 32; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
+    if (SPLIT > 1) {
+        // Publish this piece's statistics; the row's last CTA to arrive merges all of them (in
+        // piece order) and resets the row's counter for the next launch.
+        RowPart *parts = P.piece + (size_t)row * SPLIT;
+        int last = 0;
+        if (lane == 0) {
+            parts[piece] = RowPart{p.m, p.s, p.arg, p.flags};
+            __threadfence();
+            last = atomicAdd(&P.count[row], 1) == SPLIT - 1;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence();
+        p = Part{-INFINITY, 0.f, kNone, 0};
+        if (lane < SPLIT) {
+            const volatile RowPart *vp = parts + lane;   // written by other CTAs: bypass L1
+            p = Part{vp->m, vp->s, vp->arg, vp->flags};
+        }
+        // full butterfly: every lane of warp 0 needs the row's statistics (child gathers)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
+        if (lane == 0) P.count[row] = 0;
+    }
 
     if (MODE != ROW_PROBS) {
         if (p.m == INFINITY) p.flags |= F_POSINF;
@@ -207,8 +232,30 @@ cudaError_t launch_pair_d(const RowStatsParams &a, const RowStatsParams &b, int 
     return launch_pair<DT1, 0, ROW_SAMPLE>(a, b, st);
 }
 
+// Small batches: SPLIT CTAs per row (each streaming kRowChunks / SPLIT chunks) so that one
+// wave of CTAs covers the GPU.
+template <int DT, int MODE, int SPLIT>
+__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS)
+    row_stats_split_kernel(RowStatsParams P) {
+    grid_dep_wait();
+    grid_dep_launch();
+    row_stats_row<DT, MODE, false, SPLIT>(P, 0);
+}
+
 template <int DT, int MODE>
 cudaError_t launch(const RowStatsParams &p, cudaStream_t st) {
+    if (p.piece && p.count) {
+        const dim3 block(kThreads);
+        if (p.split == 8)
+            return launch_dependent(row_stats_split_kernel<DT, MODE, 8>, dim3(p.rows * 8), block,
+                                    0, st, p);
+        if (p.split == 4)
+            return launch_dependent(row_stats_split_kernel<DT, MODE, 4>, dim3(p.rows * 4), block,
+                                    0, st, p);
+        if (p.split == 2)
+            return launch_dependent(row_stats_split_kernel<DT, MODE, 2>, dim3(p.rows * 2), block,
+                                    0, st, p);
+    }
     return launch_dependent(row_stats_kernel<DT, MODE>, dim3(p.rows), dim3(kThreads), 0, st, p);
 }
 

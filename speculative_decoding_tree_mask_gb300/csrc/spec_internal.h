@@ -63,6 +63,13 @@ __host__ __device__ __forceinline__ int row_chunk_vec(int c, int nv, int64_t V, 
 }
 enum DraftKind { DRAFT_POINT = 0, DRAFT_PROBS_F32 = 1, DRAFT_LOGITS = 2 };
 
+// Partial statistics of a piece of a row: max, sum of 2^((x - max) k), lowest index of the
+// max, flags.
+struct RowPart {
+    float m, s;
+    int arg, flags;
+};
+
 // Row statistics over `rows` rows of V elements (see spec_row_stats in spec_verify.h).
 struct RowStatsParams {
     const void *x;
@@ -81,6 +88,12 @@ struct RowStatsParams {
     int pc_normalized;       // 1: pc = e_t / S (probability); 0: pc = e_t (walk input)
     const int32_t *n_active = nullptr;   // per-request node budget [B]; null = all N rows
     float2 *chunk = nullptr;   // sampling: (max, sum) of each row chunk [rows, kRowChunks]
+    // Small batches: with piece and count set and split in {2, 4, 8}, each row is streamed by
+    // `split` CTAs; piece holds their partial statistics [rows, split], count their arrivals
+    // [rows] (zero between launches).
+    RowPart *piece = nullptr;
+    int32_t *count = nullptr;
+    int split = 1;
 };
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);

@@ -177,6 +177,35 @@ def test_row_stats_against_oracle(h, orc, T, dtype, V):
             assert abs(pc[b, c] - p) <= 1e-5 * p + 1e-30, (b, c, pc[b, c], p)
 
 
+
+@pytest.mark.parametrize("B", [1, 6, 12, 24, 60])
+@pytest.mark.parametrize("dtype,V", [("bf16", 151936), ("f32", 4099)])
+def test_row_stats_every_row_split(h, orc, B, dtype, V):
+    """Few rows are streamed by several CTAs each (8, 4 or 2 pieces, merged by the last CTA to
+    finish): 16-node requests give 16 to 960 rows, across every split of a 152-SM GPU and the
+    unsplit kernel. Repeated calls check that the per-row arrival counters start from zero."""
+    w = W.WORKLOADS["sampling_trie"].scaled(B=B, N=16, V=V, dtype=dtype, seed=B * 7 + V)
+    x = W.make(w, device=DEV)
+    rows = w.B * w.N
+    hl = PY.host(x["logits"]).reshape(rows, V)
+    ref = [orc.row_stats(hl[r], 1.0) for r in range(rows)]
+    for T, rep in ((1.0, 0), (1.0, 1), (0.0, 0)):
+        m = torch.empty(rows, device=DEV)
+        s = torch.empty(rows, device=DEV)
+        a = torch.empty(rows, dtype=torch.int32, device=DEV)
+        f = torch.empty(rows, dtype=torch.int32, device=DEV)
+        G.spec_row_stats(h, x["logits"], w.N, T, m, s, a, f)
+        torch.cuda.synchronize()
+        m, s, a, f = (t.cpu().numpy() for t in (m, s, a, f))
+        assert not f.any()
+        for r in range(rows):
+            om, oS, oa, _ = ref[r]
+            assert m[r] == om and a[r] == oa, (T, rep, r)
+            if T > 0:
+                assert abs(s[r] - oS) <= 1e-5 * oS, (rep, r, s[r], oS)
+            else:
+                assert s[r] == 0.0, r
+
 # ---- sampling, point-mass drafts ----------------------------------------------------------------
 
 @pytest.mark.parametrize("T,boost", [(0.7, 8.0), (0.7, 30.0), (1.0, 12.0), (1.8, 20.0)])
