@@ -32,6 +32,7 @@ struct spec_ctx {
     RowPart *piece = nullptr;             // small batches: per-piece row statistics
     int32_t *count = nullptr;             // ... and per-row arrivals (zero between calls)
     int slots = 0;                        // CTAs of the row-statistics kernel in one wave
+    int sms = 0;                          // streaming multiprocessors of the device
     const int32_t *n_active = nullptr;   // node budget set by spec_set_node_budget
     bool prof = false;
     bool ev_ready = false;
@@ -123,6 +124,17 @@ void set_split(spec_handle h, RowStatsParams &rp) {
             rp.split = s;
             break;
         }
+}
+
+// Dense drafts, few requests: run each request's walk on a cluster of the most CTAs (8, 4 or
+// 2) that still fit one wave of the walk kernel (one CTA per SM), so that its full-row passes
+// over the target and draft rows are spread over that many SMs. Point drafts keep one CTA.
+int walk_cluster(spec_handle h, int B, bool point) {
+    if (point) return 1;
+    const int64_t wave = h->sms;
+    for (int c = 8; c > 1; c /= 2)
+        if ((int64_t)B * c <= wave) return c;
+    return 1;
 }
 
 WalkOutputs outputs(int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
@@ -233,6 +245,7 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
         return SPEC_ERR_CUDA;
     }
     h->slots = 6 * sms;   // the row-statistics kernel keeps 6 CTAs on every SM
+    h->sms = sms;
     *out = h;
     return SPEC_OK;
 }
@@ -378,6 +391,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     wp.out = out;
     wp.n_active = h->n_active;
     wp.chunk = draft_kind == SPEC_DRAFT_POINT ? h->chunk : nullptr;
+    wp.cluster = walk_cluster(h, B, draft_kind == SPEC_DRAFT_POINT);
     return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
 }
 

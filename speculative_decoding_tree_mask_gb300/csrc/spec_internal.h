@@ -27,6 +27,28 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// The same for a kernel launched in thread-block clusters of `cluster` CTAs along x.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent_cluster(void (*kernel)(Params...), dim3 grid, dim3 block,
+                                     size_t smem, cudaStream_t st, int cluster,
+                                     Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)
 
 enum RowMode { ROW_GREEDY = 0, ROW_SAMPLE = 1, ROW_PROBS = 2 };
@@ -157,6 +179,9 @@ struct SampleWalkParams {
     WalkOutputs out;
     const int32_t *n_active = nullptr;
     const float2 *chunk = nullptr;   // row-chunk partials of the target rows (eager, may be null)
+    // Eager walks: CTAs per request (1, 2, 4 or 8), one thread-block cluster each; the
+    // cluster splits every vocabulary pass of its request.
+    int cluster = 1;
 };
 
 // KV commit of the accepted path into a paged cache (see spec_kv_commit).

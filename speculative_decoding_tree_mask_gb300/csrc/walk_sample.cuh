@@ -43,6 +43,9 @@
 namespace specv {
 namespace {
 
+#ifndef SPEC_DENSE_PASS_UNROLL
+#define SPEC_DENSE_PASS_UNROLL 2   // sub-tiles in flight per warp in a dense-draft pass
+#endif
 #ifndef SPEC_LAZY_UNROLL
 #define SPEC_LAZY_UNROLL 6   // 16-byte loads in flight per thread in the lazy row pass
 #endif
@@ -76,7 +79,25 @@ struct Smem {
     float2 epart[kMaxN][kRowChunks];   // eager point drafts: chunk partials of every node's row
     int wflag[kWarps];
     rowpass::Part part[kWarps], part_out;
+    double ctot;   // clusters: this CTA's share of a pass total
+    int bcast;     // clusters: a control value of the leading CTA
 };
+
+// Clusters (CL CTAs per request): every CTA runs the same walk on the same data, but each
+// branch that is followed by a cluster barrier takes the leading CTA's value, so all CTAs
+// pass the same barriers even if their own values differed. `v` is block-uniform.
+template <int CL>
+__device__ __forceinline__ int lead(Smem &sm, int v) {
+    if constexpr (CL == 1) {
+        return v;
+    } else {
+        if (threadIdx.x == 0) sm.bcast = v;
+        cluster_sync();
+        const int r = ld_cluster_s32(cluster_addr(&sm.bcast, 0));
+        cluster_sync();
+        return r;
+    }
+}
 
 struct Ctx {
     const char *zrow;    // target row of the node
@@ -217,25 +238,31 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
 
 // Every warp sums its sub-tiles of [jlo, jhi) (default: the whole row) into subsum[] (one warp
 // scan per 256 elements); with `total`, their sum lands in sm.total. All threads call it; it
-// ends synchronised.
-template <int DT, int DK, int DDT>
+// ends synchronised. With clusters (CL > 1) the CL * 16 warps of the cluster share the
+// sub-tiles (warp w of CTA r takes those with (j - jlo) mod 16 CL = 16 r + w); afterwards every
+// CTA holds all of the range's sub-tile sums and the same total (CTA shares added in rank
+// order).
+template <int DT, int DK, int DDT, int CL = 1>
 __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0,
                               int jhi = INT_MAX, bool total = true) {
     // sub-tiles in flight per warp (32 registers of raw loads)
-    constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : 2;
+    constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : SPEC_DENSE_PASS_UNROLL;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
+    constexpr int GW = CL * kWarps;   // warps sharing the pass
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rank = CL == 1 ? 0 : cluster_rank();
+    const int gw = rank * kWarps + warp;
     const int nsub = min((c.V + kSub - 1) / kSub, jhi);
     const bool vec = c.zvec && (DK == DRAFT_POINT || !c.useq || c.dvec);
     const int nfull = min(vec ? c.V / kSub : 0, nsub);
     KSum wsum;
     int rc = 0;
 
-    for (int j0 = jlo + warp; j0 < nfull; j0 += kWarps * U) {
+    for (int j0 = jlo + gw; j0 < nfull; j0 += GW * U) {
         uint4 za[U], zb[U], da[U], db[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * kWarps;
+            const int j = j0 + u * GW;
             if (j < nfull) {
                 const int e0 = j * kSub + lane * 8;
                 fetch<DT>(c.zrow, e0, za[u], zb[u]);
@@ -244,7 +271,7 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * kWarps;
+            const int j = j0 + u * GW;
             if (j < nfull) {
                 float zs[8], ds[8], r[8];
                 shifted8<DT>(za[u], zb[u], c.negm, zs);
@@ -261,7 +288,13 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
         }
     }
     // Ragged last sub-tile, or every sub-tile of a row that is not 16-byte aligned.
-    for (int j = max(nfull, jlo) + warp; j < nsub; j += kWarps) {
+    int j1 = max(nfull, jlo) + warp;
+    if (CL > 1) {   // keep the cluster's assignment of sub-tiles to warps
+        j1 = jlo + gw;
+        const int start = max(nfull, jlo);
+        if (j1 < start) j1 += (start - j1 + GW - 1) / GW * GW;
+    }
+    for (int j = j1; j < nsub; j += GW) {
         float r[8];
         residual8_any<DT, DK, DDT>(c, sm, j, lane, rc, r);
         const float incl = warp_incl_scan(sum8(r));
@@ -271,19 +304,39 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
         }
     }
 
-    if (!total) {
+    if (!total && CL == 1) {
         __syncthreads();
         return;
     }
-    if (lane == 31) sm.wtot[warp] = wsum.value();
+    if (total && lane == 31) sm.wtot[warp] = wsum.value();
     __syncthreads();
-    if (warp == 0) {
+    if (total && warp == 0) {
         double t = lane < kWarps ? sm.wtot[lane] : 0.0;
 #pragma unroll
         for (int o = kWarps / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) sm.total = t;
+        if (lane == 0) {
+            if (CL == 1)
+                sm.total = t;
+            else
+                sm.ctot = t;
+        }
     }
-    __syncthreads();
+    if (CL == 1) {
+        __syncthreads();
+        return;
+    }
+    // Clusters: gather the other CTAs' sub-tile sums and shares of the total.
+    cluster_sync();
+    for (int j = jlo + (int)threadIdx.x; j < nsub; j += kThreads) {
+        const int own = ((j - jlo) % GW) / kWarps;
+        if (own != rank) subsum[j] = ld_cluster_f32(cluster_addr(subsum + j, own));
+    }
+    if (total && threadIdx.x == 0) {
+        double t = 0.0;
+        for (int r = 0; r < CL; ++r) t += ld_cluster_f64(cluster_addr(&sm.ctot, r));
+        sm.total = t;
+    }
+    cluster_sync();
 }
 
 // Largest token with r > 0 in sub-tiles [jlo, jhi) (warp 0), from the stored sub-tile sums:
@@ -449,7 +502,11 @@ __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, f
 struct WalkState {
     unsigned long long kids;   // children of the current node not tested yet (bit = node)
     double base, sub;          // point drafts: denominator = base - sub (unnormalised e)
-    double inv_s, inv_sq;      // dense drafts: 1 / S of the node's target and draft rows
+    // Dense drafts: decisions are taken on p and q scaled by S * S_q (S, S_q: the sums of the
+    // node's target and draft rows; S_q = 1 for draft probabilities), which needs no
+    // division: p S S_q = e_t S_q and q S S_q = e_q S, both exact products in float64. The
+    // residual levels are linear in that scale, and u < r / q compares scale-free.
+    double mul_p, mul_q;
     int node, L, st, await;
     bool entering, just_summed;
     bool stats_ready;          // lazy walks: the current node's statistics are in shared memory
@@ -497,8 +554,8 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
             w.sub = 0.0;
             w.just_summed = false;
             if (DK != DRAFT_POINT && w.kids) {
-                w.inv_s = 1.0 / (double)sm.s[w.node];
-                w.inv_sq = DK == DRAFT_LOGITS ? 1.0 / (double)sm.sq[w.node] : 1.0;
+                w.mul_p = DK == DRAFT_LOGITS ? (double)sm.sq[w.node] : 1.0;
+                w.mul_q = (double)sm.s[w.node];
             }
             __syncwarp();
             if (lane == 0) {
@@ -562,8 +619,8 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
                 continue;
             }
         } else {
-            const double p = (double)sm.ec[c] * w.inv_s;
-            const double q = (double)sm.eqc[c] * w.inv_sq;
+            const double p = (double)sm.ec[c] * w.mul_p;   // p S S_q
+            const double q = (double)sm.eqc[c] * w.mul_q;  // q S S_q
             double r = p;
             const int nlev = sm.nlev;
             for (int l = 0; l < nlev; ++l)
@@ -751,14 +808,18 @@ __device__ __forceinline__ Ctx node_ctx(const SampleWalkParams &P, const Smem &s
 
 // Point drafts fit 64 registers (2 CTAs per SM); dense drafts keep more live values.
 // LAZY: no row-statistics kernel ran; the walk streams only the rows it visits.
-template <int DT, int DK, int DDT, bool LAZY>
+// CL: CTAs per request (eager walks), launched as one thread-block cluster per request; they
+// share every vocabulary pass, and the leading CTA writes the outputs.
+template <int DT, int DK, int DDT, bool LAZY, int CL = 1>
 __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     walk_sample_kernel(SampleWalkParams P) {
+    static_assert(CL == 1 || CL == 2 || CL == 4 || CL == 8, "cluster size");
+    static_assert(!LAZY || CL == 1, "lazy walks run one CTA per request");
     __shared__ Smem sm;
     extern __shared__ float subsum[];   // sub-tile sums of the current pass
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
+    const int b = CL == 1 ? (int)blockIdx.x : (int)blockIdx.x / CL;
     const int N = P.N;
     const size_t base = (size_t)b * N;
     const int nb = node_budget(P.n_active, b, N);   // nodes >= nb do not exist in this call
@@ -803,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
     WalkState w;
     w.kids = 0;
     w.base = w.sub = 0.0;
-    w.inv_s = w.inv_sq = 1.0;
+    w.mul_p = w.mul_q = 1.0;
     w.node = 0;
     w.L = 0;
     w.st = 0;
@@ -845,14 +906,14 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             }
         }
         __syncthreads();
-        cmd = sm.cmd;
+        cmd = lead<CL>(sm, sm.cmd);
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
         if (LAZY && cmd == CMD_STATS) {
             lazy_stats<DT, DK, DDT>(P, sm, base, sm.node);
             continue;
         }
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
-        residual_pass<DT, DK, DDT>(c, sm, subsum);
+        residual_pass<DT, DK, DDT, CL>(c, sm, subsum);
     }
 
     if (cmd == CMD_BONUS) {
@@ -867,32 +928,34 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             constexpr int nc = LAZY ? kLazyChunks : kRowChunks;
             const float2 *part = LAZY ? (sm.cpart_node == sm.node ? sm.cpart : nullptr)
                                       : (P.chunk ? sm.epart[sm.node] : nullptr);
+            int q = -1;
             if (part && c.zvec) {
                 if (warp == 0) chunk_pick(c, sm, part, nc, ub);
                 __syncthreads();
-                const int q = sm.cpick;
-                if (q >= 0) {
-                    const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                    residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);
-                    if (warp == 0) {
-                        const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
-                                                                sm.ctau);
-                        if (lane == 0) sm.bonus = v;
-                    }
-                    __syncthreads();
-                    drawn = sm.bonus >= 0;
+                q = sm.cpick;
+            }
+            q = lead<CL>(sm, q);
+            if (q >= 0) {
+                const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
+                residual_pass<DT, DK, DDT, CL>(c, sm, subsum, jlo, jhi, false);
+                if (warp == 0) {
+                    const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
+                                                            sm.ctau);
+                    if (lane == 0) sm.bonus = v;
                 }
+                __syncthreads();
+                drawn = lead<CL>(sm, sm.bonus) >= 0;
             }
         }
         for (int attempt = 0; attempt < 3 && !drawn; ++attempt) {
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
-            residual_pass<DT, DK, DDT>(c, sm, subsum);
+            residual_pass<DT, DK, DDT, CL>(c, sm, subsum);
             if (warp == 0) {
                 const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub);
                 if (lane == 0) sm.bonus = v;
             }
             __syncthreads();
-            if (sm.bonus >= 0) break;
+            if (lead<CL>(sm, sm.bonus) >= 0) break;
             // The residual sums to zero. Dense: the last level is degenerate (target and draft
             // agree to rounding): keep the previous level. Point: every token with mass was
             // rejected through rounding: draw from the node's target row.
@@ -909,6 +972,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         }
     }
     __syncthreads();
+    if (CL > 1 && cluster_rank() != 0) return;   // the leading CTA writes the outputs
 
     // Compaction.
     const int fst = sm.st;
@@ -939,9 +1003,28 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
     const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);   // sub-tile sums
-    if (!p.lazy)
-        return launch_dependent(walk_sample_kernel<DT, DK, DDT, false>, dim3(p.B),
-                                dim3(kThreads), smem, st, p);
+    if (!p.lazy) {
+        const dim3 block(kThreads);
+        // Point drafts pass over one chunk of the stop row at most: a cluster's barriers would
+        // cost more than splitting that pass saves, so they keep one CTA per request.
+        if constexpr (DK != DRAFT_POINT) {
+            switch (p.cluster) {
+            case 8:
+                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 8>,
+                                                dim3(p.B * 8), block, smem, st, 8, p);
+            case 4:
+                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 4>,
+                                                dim3(p.B * 4), block, smem, st, 4, p);
+            case 2:
+                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 2>,
+                                                dim3(p.B * 2), block, smem, st, 2, p);
+            default:
+                break;
+            }
+        }
+        return launch_dependent(walk_sample_kernel<DT, DK, DDT, false>, dim3(p.B), block, smem,
+                                st, p);
+    }
     walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }

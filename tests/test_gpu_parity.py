@@ -335,6 +335,56 @@ def test_dense_tree_logits(h, orc):
     PY.compare_sample(gpu, ref)
 
 
+
+@pytest.mark.parametrize("B", [3, 30, 60, 100, 200])
+@pytest.mark.parametrize("kind", ["point", "dense"])
+def test_walk_clusters(h, orc, B, kind):
+    """With dense drafts, few requests run their walk on a thread-block cluster of 8, 4 or 2
+    CTAs that share every vocabulary pass (sub-tile sums and totals exchanged through
+    distributed shared memory): 3 to 200 requests span every cluster size of a 152-SM GPU (8
+    CTAs up to 19 requests, 4 up to 38, 2 up to 76) and one CTA per request beyond. Point
+    drafts, one CTA per request, run the same batch sizes. Odd V leaves a ragged last
+    sub-tile and, for bf16 rows, rows that are not 16-byte aligned."""
+    rng = np.random.default_rng(B * 31 + len(kind))
+    N, T = 12, 1.0
+    V = 20011 if kind == "point" else 9001
+    parent = np.stack([W.random_trie(rng, N, 4, 3) for _ in range(B)])
+    gen = torch.Generator().manual_seed(B)
+    target = torch.randn((B, N, V), generator=gen) * (3.0 if kind == "point" else 1.0)
+    tok = np.zeros((B, N), np.int32)
+    draft = None
+    if kind == "point":
+        for b in range(B):
+            tok[b] = W.child_tokens(rng, parent[b], V)
+            for i in range(N):   # boost the first child (most nodes) so that walks go deep
+                kids = np.nonzero(parent[b] == i)[0]
+                if len(kids):
+                    t = int(tok[b, kids[0]]) if rng.random() < 0.7 else int(rng.integers(V))
+                    target[b, i, t] += 18.0
+    else:
+        draft = target + 0.7 * torch.randn((B, N, V), generator=gen)
+        probs = torch.softmax(draft / T, dim=-1)
+        for b in range(B):
+            for c in range(1, N):
+                tok[b, c] = int(torch.multinomial(probs[b, parent[b, c]], 1, generator=gen))
+    logits = target.to(torch.bfloat16)
+    u = torch.rand((B, N + 1), generator=gen)
+    args = (_to(logits), _to(tok), _to(parent), T, _to(u))
+    if kind == "point":
+        gpu = PY.gpu_sample(h, *args)
+        ref = PY.oracle_sample(orc, *args)
+        assert gpu["accept_len"].max() >= 2
+    else:
+        dl = draft.to(torch.bfloat16)
+        gpu = PY.gpu_sample(h, *args, _to(dl), G.SPEC_DRAFT_LOGITS)
+        ref = PY.oracle_sample(orc, *args, dl, G.SPEC_DRAFT_LOGITS)
+    PY.compare_sample(gpu, ref)
+    # the same call twice gives the same outputs
+    again = PY.gpu_sample(h, *args) if kind == "point" else \
+        PY.gpu_sample(h, *args, _to(dl), G.SPEC_DRAFT_LOGITS)
+    for k in PY.KEYS:
+        assert np.array_equal(gpu[k], again[k]), k
+
 # ---- full-size large-tree workload ----------------------------------------------------------------
 
 def test_large_tree_full_size(h, orc):
