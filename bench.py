@@ -497,6 +497,8 @@ def bench_ours(args):
     extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
                                         "dense_chain": bench_dense_chain(dev, stream, args),
                                         "small_tries": bench_small_tries(dev, stream, args),
+                                        "high_accept": bench_high_accept(h, w, mask, dev,
+                                                                         stream, args),
                                         "adaptive_budget": bench_budget(h, x, w, dev, stream,
                                                                         args)}
 
@@ -609,6 +611,82 @@ def bench_dense_chain(dev, stream, args):
                 "accept_len_mean": float(out["accept_len"].float().mean().item()),
                 "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft logits, "
                           "T=1; L2 flushed before every call"}
+
+
+def bench_high_accept(h, w, mask, dev, stream, args):
+    """The large-tree step on trees that the target mostly accepts: the same shapes with the
+    grammar token boosted by 20 instead of 8 (p of a boosted child about 0.97 at T=1), so walks
+    go several levels deep and a few requests reject a dominant token (the walk's full-row
+    re-sums). Timed like the headline step, then once more with per-kernel events."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    wd = w.scaled(boost=20.0)
+    xd = W.make(wd, device=dev, seed=wd.seed + 7919)
+    out = G.alloc_outputs(wd.B, wd.N, dev)
+    steps = min(args.steps, 500)
+
+    def step():
+        G.spec_build_tree_mask(h, xd["parent"], mask["anc_mask"], mask["depth"],
+                               mask["status"], stream)
+        G.spec_verify_sample(h, xd["logits"], xd["draft_token"], xd["parent"], wd.temperature,
+                             xd["uniforms"], out["accept_len"], out["out_tokens"],
+                             out["kv_commit"], out["bonus"], out["status"], stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    z.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(z) / steps
+    G.spec_profile_begin(h)
+    for _ in range(steps):
+        step()
+    prof = G.spec_profile_end(h)
+    # the lazy call on the same trees, one CUDA graph per step: deep walks stream more rows
+    lout = G.alloc_outputs(wd.B, wd.N, dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        def lazy_on():
+            G.spec_build_tree_mask(h, xd["parent"], mask["anc_mask"], mask["depth"],
+                                   mask["status"], side)
+            G.spec_verify_sample_lazy(h, xd["logits"], xd["draft_token"], xd["parent"],
+                                      wd.temperature, xd["uniforms"], lout["accept_len"],
+                                      lout["out_tokens"], lout["kv_commit"], lout["bonus"],
+                                      lout["status"], stream=side)
+        lazy_on()
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            lazy_on()
+    stream.wait_stream(side)
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    a2, z2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    z2.record(stream)
+    torch.cuda.synchronize(dev)
+    lms = a2.elapsed_time(z2) / steps
+    al = out["accept_len"].cpu().numpy()
+    res = {"ms_per_step": ms, "value": wd.draft_nodes / (ms / 1e3), "unit": UNIT,
+           "accept_len_mean": float(al.mean()),
+           "accept_len_hist": np.bincount(al, minlength=1).tolist(),
+           "kernels": {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
+                       for k, v in prof.items() if v[1]},
+           "lazy": {"ms_per_step": lms, "value": wd.draft_nodes / (lms / 1e3),
+                    "rows_streamed_per_step": int(lout["accept_len"].sum().item()) + wd.B,
+                    "requests_differing_from_eager": int(
+                        (lout["out_tokens"] != out["out_tokens"]).any(dim=1).sum().item())},
+           "config": f"large_tree shapes (B={wd.B} N={wd.N} V={wd.V} bf16, T=1), grammar "
+                     "token boosted by 20"}
+    del xd
+    return res
 
 
 def bench_small_tries(dev, stream, args):

@@ -74,6 +74,8 @@ struct Smem {
     int haskids;                       // lazy statistics: the node has children
     int cpick;                         // eager point bonus: chosen row chunk (-1: none)
     double ctau;                       // ... and tau relative to the chunk's start
+    unsigned cmask;                    // eager point re-sum: chunks summed exactly (bit = chunk)
+    double ckeep;                      // ... mass of the other chunks, from their partials
     int cpart_node;                    // lazy: node whose chunk partials are in cpart[]
     float2 cpart[kLazyChunks];         // lazy: (max, sum) of each chunk of that node's row
     float2 epart[kMaxN][kRowChunks];   // eager point drafts: chunk partials of every node's row
@@ -457,7 +459,9 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
 // to the chunk's start in sm.cpick / sm.ctau. The partials carry float32 rounding of the whole
 // row's mass, so when the rejected tokens held half of it or more, that rounding could move
 // tau by more than the residual's own precision: then sm.cpick = -1 and the caller sums the
-// residual over the whole row instead (as it does when no chunk has mass).
+// residual over the whole row instead (as it does when no chunk has mass). (Summing only the
+// chunks holding rejected tokens exactly, as the walk's re-sums do, was measured here: no
+// faster on deep walks and slower on the common path, whose registers it disturbed.)
 __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, float u) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -493,6 +497,33 @@ __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, f
     if (lane == 0) {
         sm.cpick = pick;
         sm.ctau = tau;
+    }
+    __syncwarp();
+}
+
+// After a heavy rejection the residual mass of the node's row is summed exactly only where it
+// has to be: over the chunks holding rejected tokens (marked in sm.cmask), while the other
+// chunks' mass comes from their partials (float32 rounding of their own, untouched mass),
+// summed into sm.ckeep (warp 0).
+__device__ void chunk_marks(const Ctx &c, Smem &sm, const float2 *part, int nc) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    double P = 0.0;
+    bool has = false;
+    if (lane < nc) {
+        const float2 pq = part[lane];
+        const int lo = row_chunk_sub(lane, c.V, nc) * kSub;
+        const int hi = lane == nc - 1 ? c.V : row_chunk_sub(lane + 1, c.V, nc) * kSub;
+        P = pq.y > 0.f ? (double)(pq.y * ex2((pq.x + c.negm) * c.k)) : 0.0;
+        for (int i = 0; i < sm.nR; ++i) has |= sm.R[i] >= lo && sm.R[i] < hi;
+    }
+    const unsigned marks = __ballot_sync(full, has);
+    double keep = has ? 0.0 : P;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) keep += __shfl_xor_sync(full, keep, o);
+    if (lane == 0) {
+        sm.cmask = marks;
+        sm.ckeep = keep;
     }
     __syncwarp();
 }
@@ -806,6 +837,17 @@ __device__ __forceinline__ Ctx node_ctx(const SampleWalkParams &P, const Smem &s
     return c;
 }
 
+// Point drafts: the chunk partials of the current node's target row, when the walk has them
+// (eager: from the row-statistics kernel; lazy: from the pass over that row) and the row is
+// 16-byte aligned; else null.
+template <bool LAZY>
+__device__ __forceinline__ const float2 *node_part(const SampleWalkParams &P, const Smem &sm,
+                                                   const Ctx &c) {
+    if (!c.zvec) return nullptr;
+    if (LAZY) return sm.cpart_node == sm.node ? sm.cpart : nullptr;
+    return P.chunk ? sm.epart[sm.node] : nullptr;
+}
+
 // Point drafts fit 64 registers (2 CTAs per SM); dense drafts keep more live values.
 // LAZY: no row-statistics kernel ran; the walk streams only the rows it visits.
 // CL: CTAs per request (eager walks), launched as one thread-block cluster per request; they
@@ -913,38 +955,69 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             continue;
         }
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
-        residual_pass<DT, DK, DDT, CL>(c, sm, subsum);
+        // Eager point drafts (a heavy rejection): re-sum only the chunks holding rejected
+        // tokens, one pass per chunk, the other chunks from their partials. One call site for
+        // every pass keeps the walk's registers from spilling. (Lazy walks re-sum the whole
+        // row: the extra state spilled in their pass loop and slowed every lazy call.)
+        constexpr int nc = LAZY ? kLazyChunks : kRowChunks;
+        unsigned mk = 0;
+        if constexpr (DK == DRAFT_POINT && !LAZY) {
+            const float2 *part = node_part<LAZY>(P, sm, c);
+            if (part) {
+                if (warp == 0) chunk_marks(c, sm, part, nc);
+                __syncthreads();
+                mk = sm.cmask;
+                if (__popc(mk) > 2) mk = 0;   // more chunk passes than one row pass would cost
+            }
+        }
+        const bool chunked = mk != 0;
+        double acc = chunked ? sm.ckeep : 0.0;
+        do {
+            int jlo = 0, jhi = INT_MAX;
+            if (chunked) {
+                const int q = __ffs(mk) - 1;
+                mk &= mk - 1;
+                jlo = row_chunk_sub(q, c.V, nc);
+                jhi = row_chunk_sub(q + 1, c.V, nc);
+            }
+            residual_pass<DT, DK, DDT, CL>(c, sm, subsum, jlo, jhi);
+            acc += sm.total;
+        } while (mk);
+        if (chunked) {
+            __syncthreads();   // every thread has read the last pass's total
+            if (tid == 0) sm.total = acc;
+            __syncthreads();
+        }
     }
 
     if (cmd == CMD_BONUS) {
         const float ub = sm.u[N];
         bool drawn = false;
-        if (DK == DRAFT_POINT) {
+        if constexpr (DK == DRAFT_POINT) {
             // One chunk instead of the row: locate the chunk from the chunk partials of the
             // stop row (the row-statistics kernel's, or those of the lazy pass over it), then
             // sum and search only its sub-tiles. Rows that are not 16-byte aligned have no
             // partials.
+            static_assert(CL == 1, "point drafts run one CTA per request");
             const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
             constexpr int nc = LAZY ? kLazyChunks : kRowChunks;
-            const float2 *part = LAZY ? (sm.cpart_node == sm.node ? sm.cpart : nullptr)
-                                      : (P.chunk ? sm.epart[sm.node] : nullptr);
+            const float2 *part = node_part<LAZY>(P, sm, c);
             int q = -1;
-            if (part && c.zvec) {
+            if (part) {
                 if (warp == 0) chunk_pick(c, sm, part, nc, ub);
                 __syncthreads();
                 q = sm.cpick;
             }
-            q = lead<CL>(sm, q);
             if (q >= 0) {
                 const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                residual_pass<DT, DK, DDT, CL>(c, sm, subsum, jlo, jhi, false);
+                residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);
                 if (warp == 0) {
                     const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
                                                             sm.ctau);
                     if (lane == 0) sm.bonus = v;
                 }
                 __syncthreads();
-                drawn = lead<CL>(sm, sm.bonus) >= 0;
+                drawn = sm.bonus >= 0;
             }
         }
         for (int attempt = 0; attempt < 3 && !drawn; ++attempt) {

@@ -246,6 +246,35 @@ def test_sample_rejected_mass_resummed(h, orc):
 
 
 @pytest.mark.parametrize("lazy", [False, True])
+@pytest.mark.parametrize("chunks", [1, 2, 4])
+def test_heavy_rejections_across_chunks(h, orc, lazy, chunks):
+    """Four children of the root hold 99.6% of the row's mass and are rejected one after
+    another. Before the fourth decision the residual is re-summed: the eager walk sums the
+    chunks holding rejected tokens exactly and takes the rest from the chunk partials when
+    there are at most two such chunks, else (and in the lazy walk) the whole row. The bonus
+    after the last rejection sums the whole row. The rejected tokens lie in one, two or four
+    of the row's chunks."""
+    B, N, V = 16, 5, 151936
+    g = torch.Generator(device=DEV)
+    g.manual_seed(23 + chunks)
+    logits = (3.0 * torch.randn((B, N, V), device=DEV, generator=g)).to(torch.bfloat16)
+    toks = {1: [1000, 1010, 1020, 1030], 2: [1000, 1010, 150000, 150010],
+            4: [1000, 150000, 70000, 40000]}[chunks]
+    for t, v in zip(toks, [22.0, 21.0, 20.0, 19.0]):
+        logits[:, 0, t] = v
+    parent = _to(np.tile(np.array([-1, 0, 0, 0, 0], np.int32), (B, 1)))
+    tok = _to(np.tile(np.array([0] + toks, np.int32), (B, 1)))
+    u = torch.rand((B, N + 1), device=DEV, generator=g)
+    u[:, 1:5] = 0.999999
+    fn = G.verify_sample_lazy if lazy else G.verify_sample
+    out = fn(h, logits, tok, parent, 1.0, u)
+    torch.cuda.synchronize()
+    gpu = PY.to_np(out)
+    ref = PY.oracle_sample(orc, logits, tok, parent, 1.0, u)
+    assert (ref["accept_len"] == 0).all()
+    PY.compare_sample(gpu, ref)
+
+@pytest.mark.parametrize("lazy", [False, True])
 @pytest.mark.parametrize("top", [20.0, 16.5, 15.0, 12.0])
 def test_bonus_after_a_heavy_rejection(h, orc, lazy, top):
     """The root's only child holds a large share of the row's mass (about 97%, 50%, 20% and 1%
