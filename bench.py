@@ -289,6 +289,17 @@ def bench_ours(args):
                 "kernel": "row_stats_kernel<bf16, sample>", "peak_source": pk_kind,
                 "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": rs_avg}
     step_bytes = alg_bytes  # logits read once per step (bonus row and metadata excluded)
+    # Secondary bound of the sampling stream: one exponential (ex2 on the special-function
+    # unit) per logit. GB300's special-function units retire 32 ex2 per SM per clock (twice
+    # the rate of the earlier Blackwell part), so the peak is SMs x 32 x max SM clock.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = pk.get("sm_max_mhz", 2070.0)
+    ex2_peak = sms * 32 * sm_mhz * 1e6 / 1e12
+    ex2_achieved = B * N * V / (rs_avg / 1e3) / 1e12
+    sfu = {"bound": "sfu", "achieved": ex2_achieved, "peak": ex2_peak, "unit": "Tex2/s",
+           "frac": ex2_achieved / ex2_peak, "kernel": "row_stats_kernel<bf16, sample>",
+           "peak_source": f"derived: {sms} SMs x 32 ex2 per clock x {sm_mhz:.0f} MHz",
+           "ex2_per_launch": B * N * V}
     kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]}
                for k, v in prof.items() if v[1]}
 
@@ -519,7 +530,9 @@ def bench_ours(args):
                 "config": config_of(w, world),
                 "logit_GBps": step_bytes / (ms / 1e3) / 1e9,
                 "logit_hbm_frac_of_measured": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
+                "rows_per_s": B * N * world / (ms / 1e3),
+                "roofline": roofline, "secondary_bound": sfu,
+                "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
                 "greedy": greedy, "lazy": lazy, **extra,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
                 "ms_per_step_with_kernel_events": ms_profiled,
