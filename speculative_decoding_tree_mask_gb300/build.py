@@ -37,13 +37,15 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile and link the library; returns its path. Rebuilds only when a source changed."""
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          nvtx: bool = False) -> str:
+    """Compile and link the library; returns its path. Rebuilds only when a source changed.
+    `nvtx` compiles an NVTX range around every ABI entry point (for timeline profilers)."""
     if not force and os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= _newest_input():
         return LIBRARY
     os.makedirs(OBJDIR, exist_ok=True)
     cc = nvcc()
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DSPEC_NVTX"] if nvtx else [])
 
     def compile_one(src):
         obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
@@ -69,5 +71,6 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None))
+    print(build(force="--force" in sys.argv or "--nvtx" in sys.argv, verbose="-v" in sys.argv,
+                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None,
+                nvtx="--nvtx" in sys.argv))

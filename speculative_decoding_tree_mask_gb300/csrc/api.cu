@@ -10,6 +10,24 @@
 #include "spec_internal.h"
 #include "spec_verify.h"
 
+// Built with SPEC_NVTX, every entry point of the ABI is an NVTX range named after it, so a
+// timeline profiler shows the host side of each call around its kernels. Otherwise the
+// ranges compile to nothing.
+#ifdef SPEC_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+}  // namespace
+#define SPEC_RANGE(name) NvtxRange spec_range_(name)
+#else
+#define SPEC_RANGE(name) ((void)0)
+#endif
+
 using namespace specv;
 
 namespace {
@@ -194,6 +212,7 @@ const char *spec_error_string(int code) {
 }
 
 int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int device) {
+    SPEC_RANGE("spec_verify_init");
     if (!out) return SPEC_ERR_ARG;
     *out = nullptr;
     if (max_B < 1 || max_N < 1 || max_V < 1) return SPEC_ERR_ARG;
@@ -251,6 +270,7 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
 }
 
 int spec_verify_destroy(spec_handle h) {
+    SPEC_RANGE("spec_verify_destroy");
     if (!h) return SPEC_OK;
     DeviceScope ds(h->device);
     if (h->ev_ready)
@@ -262,6 +282,7 @@ int spec_verify_destroy(spec_handle h) {
 
 int spec_build_tree_mask(spec_handle h, const int32_t *parent, int B, int N, uint64_t *anc_mask,
                          int32_t *depth, int32_t *status, void *stream) {
+    SPEC_RANGE("spec_build_tree_mask");
     if (!h) return SPEC_ERR_ARG;
     if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
     if (B == 0) return SPEC_OK;
@@ -280,6 +301,7 @@ int spec_verify_greedy(spec_handle h, const void *logits, int dtype, int B, int 
                        const int32_t *draft_token, const int32_t *parent, int32_t *accept_len,
                        int32_t *out_tokens, int32_t *kv_commit, int32_t *bonus, int32_t *status,
                        void *stream) {
+    SPEC_RANGE("spec_verify_greedy");
     int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
                           out_tokens, kv_commit, bonus, status);
     if (rc != SPEC_OK || B == 0) return rc;
@@ -295,6 +317,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
                        int draft_kind, int draft_dtype, float temperature,
                        const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
                        int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream) {
+    SPEC_RANGE("spec_verify_sample");
     int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
                           out_tokens, kv_commit, bonus, status);
     if (rc != SPEC_OK) return rc;
@@ -399,6 +422,7 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
                             int64_t V, const int32_t *draft_token, const int32_t *parent,
                             int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
                             int32_t *bonus, int32_t *status, void *stream) {
+    SPEC_RANGE("spec_verify_greedy_lazy");
     int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
                           out_tokens, kv_commit, bonus, status);
     if (rc != SPEC_OK || B == 0) return rc;
@@ -424,6 +448,7 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
                             const void *draft, int draft_kind, int draft_dtype, float temperature,
                             const float *uniforms, int32_t *accept_len, int32_t *out_tokens,
                             int32_t *kv_commit, int32_t *bonus, int32_t *status, void *stream) {
+    SPEC_RANGE("spec_verify_sample_lazy");
     int rc = check_common(h, logits, dtype, B, N, V, draft_token, parent, accept_len,
                           out_tokens, kv_commit, bonus, status);
     if (rc != SPEC_OK) return rc;
@@ -469,6 +494,7 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
 }
 
 int spec_set_node_budget(spec_handle h, const int32_t *n_active) {
+    SPEC_RANGE("spec_set_node_budget");
     if (!h) return SPEC_ERR_ARG;
     if (n_active && !aligned(n_active, 4)) return SPEC_ERR_ARG;
     h->n_active = n_active;
@@ -478,6 +504,7 @@ int spec_set_node_budget(spec_handle h, const int32_t *n_active) {
 int spec_budget_update(spec_handle h, const spec_budget_params *params,
                        const int32_t *accept_len, const int32_t *status, const int32_t *parent,
                        int B, int N, spec_budget_state *state, int32_t *n_active, void *stream) {
+    SPEC_RANGE("spec_budget_update");
     if (!h || !params || !state || !n_active) return SPEC_ERR_ARG;
     if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
     const spec_budget_params &q = *params;
@@ -511,6 +538,7 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
                    int64_t num_blocks, const int32_t *block_table, int max_blocks,
                    const int32_t *seq_pos, const float *k_scale, const float *v_scale,
                    int scale_per_token, int32_t *commit_status, void *stream) {
+    SPEC_RANGE("spec_kv_commit");
     if (!h) return SPEC_ERR_ARG;
     if (B < 0 || B > h->max_B || N < 1 || N > h->max_N || N > kMaxN) return SPEC_ERR_ARG;
     if (H < 1 || D < 1 || (int64_t)H * D > (int64_t(1) << 24)) return SPEC_ERR_ARG;
@@ -575,6 +603,7 @@ int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N
                    float temperature, const int32_t *draft_token, const int32_t *parent,
                    float *row_max, float *row_sum, int32_t *row_argmax, int32_t *row_flags,
                    float *child_prob, void *stream) {
+    SPEC_RANGE("spec_row_stats");
     if (!h) return SPEC_ERR_ARG;
     if (rows < 0 || N < 1 || N > kMaxN || V < 1 || V > kMaxV) return SPEC_ERR_ARG;
     if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_ARG;

@@ -70,3 +70,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(G, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         G.load()
+
+
+def test_nvtx_ranges_compile(tmp_path):
+    """The NVTX-instrumented flavour of the entry points (SPEC_NVTX) compiles; a range opens
+    and closes around each call without touching its arguments."""
+    import subprocess
+    obj = tmp_path / "api_nvtx.o"
+    r = subprocess.run([B.nvcc(), *B.ARCH, *B.FLAGS, "-DSPEC_NVTX", "-I", B.INCLUDE, "-I",
+                        B.CSRC, "-c", os.path.join(B.CSRC, "api.cu"), "-o", str(obj)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert obj.stat().st_size > 0
+    src = open(os.path.join(B.CSRC, "api.cu")).read()
+    for name in _declared() - {"spec_error_string", "spec_profile_begin", "spec_profile_end",
+                               "spec_verify_greedy_noalloc"}:
+        assert f'SPEC_RANGE("{name}")' in src, name
