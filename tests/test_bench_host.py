@@ -1,0 +1,93 @@
+"""Host-side helpers of bench.py on CPU: the clock record, the DRAM-traffic record that goes
+stale with the kernel's sources, the roofline peak and its fallback, and the JSON config."""
+import json
+import os
+import shutil
+
+import pytest
+
+import bench
+from speculative_decoding_tree_mask_gb300 import workloads as W
+
+
+def test_clock_summary_median_max_and_reasons():
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "1980, 2070, 1210.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2070, 2070, 1300.2, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",   # unreadable
+        "garbage",
+    ]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    s.lines.append("1400, 2070, 1390, 0x8, Active, Not Active, Active, Not Active")
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples():
+    out = bench.ClockSampler(0).summary()
+    assert out == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def _copy_tree(tmp_path):
+    """A scratch copy of the kernel sources and the traffic record, with bench pointed at it."""
+    root = tmp_path / "repo"
+    shutil.copytree(os.path.join(bench.ROOT, "speculative_decoding_tree_mask_gb300", "csrc"),
+                    root / "speculative_decoding_tree_mask_gb300" / "csrc")
+    shutil.copytree(os.path.join(bench.ROOT, "profiles"), root / "profiles")
+    return root
+
+
+def test_traffic_record_goes_stale_with_its_sources(tmp_path, monkeypatch):
+    root = _copy_tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    rec_path = root / "profiles" / "traffic.json"
+    recs = json.loads(rec_path.read_text())
+    rec = recs["row_stats.cu"]
+    # a record taken from the current sources is reported
+    rec["source_sha"] = bench.source_sha(rec["sources"])
+    rec_path.write_text(json.dumps(recs))
+    assert bench.traffic_record("row_stats.cu") == rec["bytes_per_launch"]
+    # any change to one of the kernel's files (a header included) makes it stale
+    hdr = root / "speculative_decoding_tree_mask_gb300" / "csrc" / rec["sources"][-1]
+    hdr.write_text(hdr.read_text() + "\n// edited\n")
+    assert bench.traffic_record("row_stats.cu") is None
+    # kernels without a record, and no record file at all
+    assert bench.traffic_record("no_such_kernel.cu") is None
+    rec_path.unlink()
+    assert bench.traffic_record("row_stats.cu") is None
+
+
+def test_committed_traffic_record_names_existing_sources():
+    recs = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    for name, rec in recs.items():
+        assert name in rec["sources"]
+        for f in rec["sources"]:
+            assert os.path.exists(os.path.join(bench.ROOT, "speculative_decoding_tree_mask_gb300",
+                                               "csrc", f)), f
+        assert rec["bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+        assert rec["bytes_per_launch"] >= rec["algorithmic_bytes_per_launch"]
+
+
+def test_peaks_measured_then_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    pk, kind = bench.peaks()
+    assert kind == "fallback" and pk["hbm_gbs"] == bench.FALLBACK_HBM_GBS
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6779.7}))
+    pk, kind = bench.peaks()
+    assert kind == "measured" and pk["hbm_gbs"] == 6779.7
+
+
+@pytest.mark.parametrize("world", [1, 4])
+def test_config_names_the_workload(world):
+    w = W.WORKLOADS[bench.WORKLOAD]
+    cfg = bench.config_of(w, world)
+    assert cfg["workload"].startswith("large_tree: B=256 N=64 V=152064 bf16")
+    assert cfg["global_batch"] == 256 * world
+    assert cfg["nodes_per_request"] == 64 and cfg["vocab"] == 152064
+    assert "4.98 GB" in cfg["l2"]
+    assert not {"model", "seq_len"} & set(cfg)
+    assert bench.aggregate_throughput(world, w.draft_nodes, 0.5) == world * 256 * 63 / 5e-4
