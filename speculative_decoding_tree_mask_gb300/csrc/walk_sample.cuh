@@ -1081,18 +1081,24 @@ cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
         // Point drafts pass over one chunk of the stop row at most: a cluster's barriers would
         // cost more than splitting that pass saves, so they keep one CTA per request.
         if constexpr (DK != DRAFT_POINT) {
-            switch (p.cluster) {
-            case 8:
-                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 8>,
-                                                dim3(p.B * 8), block, smem, st, 8, p);
-            case 4:
-                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 4>,
-                                                dim3(p.B * 4), block, smem, st, 4, p);
-            case 2:
-                return launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 2>,
-                                                dim3(p.B * 2), block, smem, st, 2, p);
-            default:
-                break;
+            if (p.cluster > 1) {
+                cudaError_t e;
+                if (p.cluster == 8)
+                    e = launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 8>,
+                                                 dim3(p.B * 8), block, smem, st, 8, p);
+                else if (p.cluster == 4)
+                    e = launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 4>,
+                                                 dim3(p.B * 4), block, smem, st, 4, p);
+                else
+                    e = launch_dependent_cluster(walk_sample_kernel<DT, DK, DDT, false, 2>,
+                                                 dim3(p.B * 2), block, smem, st, 2, p);
+                // A device or partition that cannot co-schedule the cluster refuses its launch
+                // configuration (nothing was launched): clear that error and run one CTA per
+                // request instead. Other errors are returned.
+                if (e != cudaErrorNotSupported && e != cudaErrorInvalidClusterSize &&
+                    e != cudaErrorLaunchOutOfResources)
+                    return e;
+                cudaGetLastError();
             }
         }
         return launch_dependent(walk_sample_kernel<DT, DK, DDT, false>, dim3(p.B), block, smem,
