@@ -49,7 +49,7 @@ typedef struct spec_ctx *spec_handle;
 enum {
     SPEC_OK = 0,
     SPEC_ERR_ARG = -1,          /* an argument is invalid or outside the handle's limits */
-    SPEC_ERR_UNSUPPORTED = -2,  /* a valid request this build does not implement */
+    SPEC_ERR_UNSUPPORTED = -2,  /* a valid request the library does not implement */
     SPEC_ERR_CUDA = -3,         /* a CUDA call or launch failed */
     SPEC_ERR_WORKSPACE = -4     /* workspace allocation failed */
 };
