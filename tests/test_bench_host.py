@@ -1,5 +1,6 @@
 """Host-side helpers of bench.py on CPU: the clock record, the DRAM-traffic record that goes
-stale with the kernel's sources, the roofline peak and its fallback, and the JSON config."""
+stale with the kernel's sources, the roofline peak and its fallback, the JSON config, and the
+reference arm's time budget."""
 import json
 import os
 import shutil
@@ -91,3 +92,23 @@ def test_config_names_the_workload(world):
     assert "4.98 GB" in cfg["l2"]
     assert not {"model", "seq_len"} & set(cfg)
     assert bench.aggregate_throughput(world, w.draft_nodes, 0.5) == world * 256 * 63 / 5e-4
+
+
+def test_reference_arm_samples_requests_to_its_budget(monkeypatch, capsys):
+    """The reference arm (the oracle) keeps its whole run near its time budget: past it, each
+    step verifies only the first requests of the batch, and the line says how many."""
+    import argparse
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = argparse.Namespace(requests=3, steps=2, warmup=1)
+    monkeypatch.setattr(bench, "REF_BUDGET_S", 1e9)
+    bench.bench_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == bench.UNIT
+    assert "first 3 of the 3 requests" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["value"] == line["value"] > 0
+    monkeypatch.setattr(bench, "REF_BUDGET_S", 1e-9)
+    bench.bench_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert "first 1 of the 3 requests" in line["cpu_baseline"]["sample"]
+    assert line["value"] > 0
