@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -91,13 +92,21 @@ def peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and with whitespace collapsed: what the compiler
+    sees (the sources hold no string literal with a comment marker in it)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_sha(files) -> str:
-    """Hash of the kernel's source files (the .cu and every header it includes)."""
+    """Hash of the code of the kernel's source files (the .cu and every header it includes),
+    comments left out: a comment edit does not change the kernel."""
     h = hashlib.sha256()
     for name in files:
-        with open(os.path.join(ROOT, "speculative_decoding_tree_mask_gb300", "csrc", name),
-                  "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "speculative_decoding_tree_mask_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

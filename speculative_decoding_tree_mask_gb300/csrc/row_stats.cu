@@ -151,8 +151,9 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
 #pragma unroll
     for (int o = kWarpsPerGroup; o < 32; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
     if (SPLIT > 1) {
-        // Publish this piece's statistics; the row's last CTA to arrive merges all of them (in
-        // piece order) and resets the row's counter for the next launch.
+        // Publish this piece's statistics; the row's last CTA to arrive merges all of them (a
+        // fixed merge tree over the pieces, so the result does not depend on which CTA is
+        // last) and resets the row's counter for the next launch.
         RowPart *parts = P.piece + (size_t)row * SPLIT;
         int last = 0;
         if (lane == 0) {

@@ -52,9 +52,12 @@ def test_traffic_record_goes_stale_with_its_sources(tmp_path, monkeypatch):
     rec["source_sha"] = bench.source_sha(rec["sources"])
     rec_path.write_text(json.dumps(recs))
     assert bench.traffic_record("row_stats.cu") == rec["bytes_per_launch"]
-    # any change to one of the kernel's files (a header included) makes it stale
+    # a comment edit leaves the kernel, and the record, as they were
     hdr = root / "speculative_decoding_tree_mask_gb300" / "csrc" / rec["sources"][-1]
-    hdr.write_text(hdr.read_text() + "\n// edited\n")
+    hdr.write_text(hdr.read_text() + "\n// a remark\n/* and\n another */\n")
+    assert bench.traffic_record("row_stats.cu") == rec["bytes_per_launch"]
+    # a code change in any of the kernel's files (a header included) makes it stale
+    hdr.write_text(hdr.read_text() + "\nconstexpr int kEdited = 1;\n")
     assert bench.traffic_record("row_stats.cu") is None
     # kernels without a record, and no record file at all
     assert bench.traffic_record("no_such_kernel.cu") is None
@@ -112,3 +115,10 @@ def test_reference_arm_samples_requests_to_its_budget(monkeypatch, capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert "first 1 of the 3 requests" in line["cpu_baseline"]["sample"]
     assert line["value"] > 0
+
+
+def test_code_only_drops_comments_and_layout():
+    a = "int f(int x) {  // doubles\n    return 2 * x; /* fast\n path */ }\n"
+    b = "int f(int x) {\n return 2 * x; }"
+    assert bench._code_only(a) == bench._code_only(b) == "int f(int x) { return 2 * x; }"
+    assert bench._code_only(a) != bench._code_only(a.replace("2 * x", "3 * x"))
