@@ -181,6 +181,8 @@ class ClockSampler:
 
 
 def run_oracle_sample(x, w, nthreads: int, reps_target_s: float = 10.0, max_reps: int = 5):
+    """The oracle over the whole batch, repeated for about reps_target_s: (draft nodes/s,
+    repetitions, seconds, the oracle's outputs)."""
     from oracle import oracle as O
     orc = O.default()
     logits = W.host_logits(x["logits"])
@@ -188,13 +190,50 @@ def run_oracle_sample(x, w, nthreads: int, reps_target_s: float = 10.0, max_reps
     t0 = time.perf_counter()
     reps = 0
     while True:
-        orc.verify_sample(logits, x["tok_np"], x["parent_np"], w.temperature, u,
-                          nthreads=nthreads)
+        ref = orc.verify_sample(logits, x["tok_np"], x["parent_np"], w.temperature, u,
+                                nthreads=nthreads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= reps_target_s or reps >= max_reps:
             break
-    return reps * w.draft_nodes / el, reps, el
+    return reps * w.draft_nodes / el, reps, el, ref
+
+
+OUT_KEYS = ("accept_len", "out_tokens", "kv_commit", "bonus", "status")
+MARGIN = 1e-6
+
+
+def parity_summary(gpu: dict, ref: dict) -> dict:
+    """Request-by-request agreement of the GPU's outputs with the oracle's on the same batch.
+    A request whose accept decision lies within MARGIN of the oracle's threshold is counted
+    apart (float32 against float64 may decide it either way). A request whose bonus draw lies
+    within MARGIN of a CDF boundary must match in everything but the bonus, and its bonus must
+    lie in the oracle's draw window [cdf_lo, cdf_hi]."""
+    B = len(ref["accept_len"])
+    excl = np.asarray(ref["decision_margin"]) < MARGIN
+    near = (np.asarray(ref["cdf_margin"]) < MARGIN) & ~excl
+    identical = np.ones(B, bool)
+    for k in OUT_KEYS:
+        identical &= np.asarray(gpu[k]).reshape(B, -1).__eq__(
+            np.asarray(ref[k]).reshape(B, -1)).all(1)
+    near_ok = np.zeros(B, bool)
+    for i in np.nonzero(near & ~identical)[0]:
+        L = int(ref["accept_len"][i])
+        same = all(np.array_equal(np.asarray(gpu[k])[i], np.asarray(ref[k])[i])
+                   for k in ("accept_len", "kv_commit", "status"))
+        g_out, r_out = np.array(gpu["out_tokens"][i]), np.array(ref["out_tokens"][i])
+        gb = int(gpu["bonus"][i])
+        g_out[L] = r_out[L]
+        near_ok[i] = (same and np.array_equal(g_out, r_out) and
+                      int(ref["cdf_lo"][i]) <= gb <= int(ref["cdf_hi"][i]) and
+                      int(gpu["out_tokens"][i][L]) == gb)
+    agree = identical | near_ok
+    return {"requests": B, "identical": int(identical.sum()),
+            "near_boundary_in_window": int((near_ok & ~identical).sum()),
+            "decision_margin_cases": int(excl.sum()),
+            "decision_margin_differing": int((excl & ~agree).sum()),
+            "mismatched": int((~agree & ~excl).sum()),
+            "margin": MARGIN}
 
 
 def bench_reference(args):
@@ -536,10 +575,15 @@ def bench_ours(args):
     cpu = None
     if rank == 0 and not args.skip_cpu_baseline:
         nthreads = os.cpu_count() or 1
-        cval, reps, el = run_oracle_sample(x, w, nthreads)
+        cval, reps, el, oref = run_oracle_sample(x, w, nthreads)
         cpu = {"value": cval, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                "sample": f"the whole {WORKLOAD} batch ({w.B} requests) x{reps} "
                          f"({el:.1f} s), float64 C oracle, OpenMP over requests"}
+        # the same batch's outputs from the timed GPU steps against the oracle's
+        try:
+            cpu["parity"] = parity_summary({k: out[k].cpu().numpy() for k in OUT_KEYS}, oref)
+        except Exception as e:   # the line is printed whatever happens here
+            cpu["parity"] = {"error": repr(e)[:200]}
 
     hist = np.bincount(out["accept_len"].cpu().numpy(), minlength=1).tolist()
     if rank == 0:

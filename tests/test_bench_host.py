@@ -5,6 +5,7 @@ import json
 import os
 import shutil
 
+import numpy as np
 import pytest
 
 import bench
@@ -122,3 +123,55 @@ def test_code_only_drops_comments_and_layout():
     b = "int f(int x) {\n return 2 * x; }"
     assert bench._code_only(a) == bench._code_only(b) == "int f(int x) { return 2 * x; }"
     assert bench._code_only(a) != bench._code_only(a.replace("2 * x", "3 * x"))
+
+
+def _ref_and_gpu():
+    rng = np.random.default_rng(3)
+    B, N = 6, 5
+    ref = {"accept_len": np.array([0, 1, 2, 0, 3, 1], np.int32),
+           "out_tokens": rng.integers(0, 100, (B, N)).astype(np.int32),
+           "kv_commit": rng.integers(0, N, (B, N)).astype(np.int32),
+           "bonus": rng.integers(0, 100, B).astype(np.int32),
+           "status": np.zeros(B, np.int32),
+           "decision_margin": np.full(B, 1.0), "cdf_margin": np.full(B, 1.0)}
+    for b in range(B):
+        ref["out_tokens"][b, ref["accept_len"][b]] = ref["bonus"][b]
+    ref["cdf_lo"], ref["cdf_hi"] = ref["bonus"] - 1, ref["bonus"] + 1
+    gpu = {k: ref[k].copy() for k in bench.OUT_KEYS}
+    return ref, gpu
+
+
+def test_parity_summary_counts():
+    ref, gpu = _ref_and_gpu()
+    s = bench.parity_summary(gpu, ref)
+    assert (s["requests"], s["identical"], s["mismatched"]) == (6, 6, 0)
+    # request 1: bonus one token off, near a CDF boundary and inside the window
+    ref["cdf_margin"][1] = 1e-8
+    L = ref["accept_len"][1]
+    gpu["bonus"][1] += 1
+    gpu["out_tokens"][1, L] += 1
+    # request 2: an accept decision within the margin, decided the other way
+    ref["decision_margin"][2] = 1e-9
+    gpu["accept_len"][2] -= 1
+    # request 3: a plain mismatch
+    gpu["kv_commit"][3, 0] += 1
+    # request 4: near a boundary but drawn outside the window
+    ref["cdf_margin"][4] = 1e-8
+    gpu["bonus"][4] += 5
+    gpu["out_tokens"][4, ref["accept_len"][4]] += 5
+    s = bench.parity_summary(gpu, ref)
+    assert s["identical"] == 2                      # requests 0 and 5
+    assert s["near_boundary_in_window"] == 1        # request 1
+    assert (s["decision_margin_cases"], s["decision_margin_differing"]) == (1, 1)
+    assert s["mismatched"] == 2                     # requests 3 and 4
+
+
+def test_parity_summary_on_the_oracle_outputs():
+    """The CPU-baseline leg's oracle outputs carry every field the summary reads."""
+    w = W.WORKLOADS["sampling_trie"].scaled(B=3, N=8, V=300, boost=12.0, seed=7)
+    x = W.make(w, seed=7)
+    value, reps, el, ref = bench.run_oracle_sample(x, w, 2, reps_target_s=0.0, max_reps=1)
+    assert reps == 1 and value > 0
+    gpu = {k: np.array(ref[k]) for k in bench.OUT_KEYS}
+    s = bench.parity_summary(gpu, ref)
+    assert s["requests"] == 3 and s["identical"] == 3 and s["mismatched"] == 0
