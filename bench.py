@@ -125,22 +125,28 @@ def traffic_record(kernel_file: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons while running. `mark()` brackets
+    a timed region; `summary(region=True)` then takes the samples within one sampling
+    interval of it (so even a region shorter than the interval has the samples on both
+    sides of it), `summary()` every sample."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
-        self.lines = []
+        self.lines = []          # (host time, line)
+        self.region = None
+        self.first = threading.Event()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -148,9 +154,18 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def wait_first(self, timeout: float = 3.0):
+        """Wait (bounded) until the sampler has produced its first sample."""
+        if self.proc is not None:
+            self.first.wait(timeout)
+
+    def mark(self, start: float, end: float):
+        self.region = (start, end)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+            self.first.set()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -161,10 +176,15 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, region: bool = False):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lines = self.lines
+        if region and self.region is not None:
+            pad = self.interval_ms / 1e3
+            a, z = self.region[0] - pad, self.region[1] + pad
+            lines = [(t, ln) for t, ln in lines if a <= t <= z]
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -177,7 +197,8 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "interval_ms": self.interval_ms}
 
 
 def run_oracle_sample(x, w, nthreads: int, reps_target_s: float = 10.0, max_reps: int = 5):
@@ -236,6 +257,41 @@ def parity_summary(gpu: dict, ref: dict) -> dict:
             "margin": MARGIN}
 
 
+def greedy_parity(gpu: dict, ref: dict) -> dict:
+    """Greedy results must equal the oracle's bit for bit, request by request."""
+    B = len(ref["accept_len"])
+    same = np.ones(B, bool)
+    for k in OUT_KEYS:
+        same &= np.asarray(gpu[k]).reshape(B, -1).__eq__(np.asarray(ref[k]).reshape(B, -1)).all(1)
+    return {"requests": B, "identical": int(same.sum()), "mismatched": int((~same).sum())}
+
+
+def snapshot(out: dict) -> dict:
+    """Host copies of a call's outputs (taken right after the call's timed region)."""
+    return {k: out[k].cpu().numpy() for k in OUT_KEYS}
+
+
+def oracle_parity(x, w, results: dict, nthreads: int, ref: dict | None = None) -> dict:
+    """Every request of the batch `x` verified by the oracle (sampling and greedy) and
+    compared with the GPU's outputs in `results` (name -> (mode, outputs)). `ref` may hold
+    the oracle's sampling result for `x` already."""
+    from oracle import oracle as O
+    orc = O.default()
+    logits = W.host_logits(x["logits"])
+    u = x["uniforms"].cpu().numpy()
+    ref = dict(ref or {})
+    if "sample" not in ref and any(m == "sample" for m, _ in results.values()):
+        ref["sample"] = orc.verify_sample(logits, x["tok_np"], x["parent_np"], w.temperature, u,
+                                          nthreads=nthreads)
+    if any(m == "greedy" for m, _ in results.values()):
+        ref["greedy"] = orc.verify_greedy(logits, x["tok_np"], x["parent_np"],
+                                          nthreads=nthreads)
+    del logits
+    return {name: (parity_summary(g, ref["sample"]) if mode == "sample"
+                   else greedy_parity(g, ref["greedy"]))
+            for name, (mode, g) in results.items()}
+
+
 def bench_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -292,6 +348,7 @@ def bench_ours(args):
     w = W.WORKLOADS[WORKLOAD]
     if args.requests:
         w = w.scaled(B=args.requests)
+    run_clocks = ClockSampler(local).__enter__()   # the whole run, all legs
     x = W.make(w, device=dev, seed=rank_seed(w, rank))
     B, N, V, T = w.B, w.N, w.V, w.temperature
     h = G.Handle(B, N, V, local)
@@ -314,15 +371,20 @@ def bench_ours(args):
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        clocks.wait_first()
+        t_start = time.perf_counter()
         start.record(stream)
         for _ in range(args.steps):
             step()
         end.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.mark(t_start, time.perf_counter())
+        time.sleep(clocks.interval_ms / 1e3 * 1.5)   # the sample after the region
     barrier(world)
     ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, world, dev)
     value = aggregate_throughput(world, w.draft_nodes, ms)
+    outs = {"eager_sample": ("sample", snapshot(out))}
     # Per-kernel durations: the same K steps again with CUDA events around every launch (on the
     # launching stream). The events sit between the kernels, so they also stop the stages from
     # overlapping their launches; that is why the headline region above runs without them.
@@ -343,10 +405,17 @@ def bench_ours(args):
     alg_bytes = B * N * V * w.elem_bytes
     pk, pk_kind = peaks()
     achieved = alg_bytes / (rs_avg / 1e3) / 1e9
+    # The committed DRAM-traffic record was captured on the full large-tree batch: it holds
+    # only for a run of that batch (and only while the kernel's code is unchanged).
+    full_batch = B == W.WORKLOADS[WORKLOAD].B
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": traffic_record("row_stats.cu"),
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic_record("row_stats.cu") if full_batch else None,
                 "kernel": "row_stats_kernel<bf16, sample>", "peak_source": pk_kind,
                 "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": rs_avg}
+    if not full_batch:
+        roofline["traffic_note"] = (f"null: the DRAM capture covers all {W.WORKLOADS[WORKLOAD].B}"
+                                    f" requests, this run verified {B}")
     step_bytes = alg_bytes  # logits read once per step (bonus row and metadata excluded)
     # Secondary bound of the sampling stream: one exponential (ex2 on the special-function
     # unit) per logit. GB300's special-function units retire 32 ex2 per SM per clock (twice
@@ -383,6 +452,7 @@ def bench_ours(args):
     ge.record(stream)
     torch.cuda.synchronize(dev)
     gms = max_over_ranks(gs.elapsed_time(ge) / args.steps, world, dev)
+    outs["eager_greedy"] = ("greedy", snapshot(gout))
     greedy = {"value": aggregate_throughput(world, w.draft_nodes, gms), "unit": UNIT,
               "ms_per_step": gms, "logit_GBps": alg_bytes / (gms / 1e3) / 1e9,
               "path": "tree mask + spec_verify_greedy (row statistics without exponentials, "
@@ -446,6 +516,7 @@ def bench_ours(args):
         torch.cuda.synchronize(dev)
         lms = max_over_ranks(s4.elapsed_time(t4) / args.steps, world, dev)
         al = lout["accept_len"].cpu()
+        outs["lazy_sample"] = ("sample", snapshot(lout))
         ndiff = int((lout["out_tokens"] != out["out_tokens"]).any(dim=1).sum().item())
         lazy = {"value": aggregate_throughput(world, w.draft_nodes, lms), "unit": UNIT,
                 "ms_per_step": lms, "ms_per_step_direct_calls": direct_ms,
@@ -481,6 +552,7 @@ def bench_ours(args):
         t5.record(stream)
         torch.cuda.synchronize(dev)
         gl_ms = max_over_ranks(s5.elapsed_time(t5) / args.steps, world, dev)
+        outs["lazy_greedy"] = ("greedy", snapshot(lgout))
         lazy["greedy"] = {"value": aggregate_throughput(world, w.draft_nodes, gl_ms),
                           "ms_per_step": gl_ms,
                           "rows_streamed_per_step":
@@ -564,26 +636,35 @@ def bench_ours(args):
                     "path": "all logits copied host to device, then spec_verify_sample"}
 
     # f2 and f1 on their own workloads: the KV commit after a verify call, and the dense chain
+    check = rank == 0 and not args.skip_parity
     extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
-                                        "dense_chain": bench_dense_chain(dev, stream, args),
-                                        "small_tries": bench_small_tries(dev, stream, args),
+                                        "dense_chain": bench_dense_chain(dev, stream, args,
+                                                                         check),
+                                        "small_tries": bench_small_tries(dev, stream, args,
+                                                                         check),
                                         "high_accept": bench_high_accept(h, w, mask, dev,
-                                                                         stream, args),
+                                                                         stream, args, check),
                                         "adaptive_budget": bench_budget(h, x, w, dev, stream,
                                                                         args)}
 
-    cpu = None
+    nthreads = os.cpu_count() or 1
+    cpu = oref = None
     if rank == 0 and not args.skip_cpu_baseline:
-        nthreads = os.cpu_count() or 1
         cval, reps, el, oref = run_oracle_sample(x, w, nthreads)
         cpu = {"value": cval, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                "sample": f"the whole {WORKLOAD} batch ({w.B} requests) x{reps} "
                          f"({el:.1f} s), float64 C oracle, OpenMP over requests"}
-        # the same batch's outputs from the timed GPU steps against the oracle's
+    # Every request of the headline batch against the oracle: the outputs of the timed eager
+    # steps, of the greedy leg and of the two lazy legs.
+    parity = None
+    if check:
         try:
-            cpu["parity"] = parity_summary({k: out[k].cpu().numpy() for k in OUT_KEYS}, oref)
+            parity = oracle_parity(x, w, outs, nthreads, {"sample": oref} if oref else None)
+            parity["margin"] = MARGIN
         except Exception as e:   # the line is printed whatever happens here
-            cpu["parity"] = {"error": repr(e)[:200]}
+            parity = {"error": repr(e)[:200]}
+        if lazy is not None and "lazy_sample" in parity:
+            lazy["vs_oracle"] = parity["lazy_sample"]
 
     hist = np.bincount(out["accept_len"].cpu().numpy(), minlength=1).tolist()
     if rank == 0:
@@ -597,20 +678,34 @@ def bench_ours(args):
                 "rows_per_s": B * N * world / (ms / 1e3),
                 "roofline": roofline, "secondary_bound": sfu,
                 "cpu_baseline": cpu, "e2e": e2e, "e2e_copy": e2e_copy,
-                "greedy": greedy, "lazy": lazy, **extra,
+                "greedy": greedy, "lazy": lazy, "parity": parity, **extra,
                 "gpu_launches": 3 * args.steps, "kernels": kernels,
                 "ms_per_step_with_kernel_events": ms_profiled,
-                "clocks": clocks.summary(), "accept_len_hist": hist}
+                "clocks": clocks.summary(region=True), "accept_len_hist": hist}
+        run_clocks.__exit__(None, None, None)
+        line["clocks_whole_run"] = dict(
+            run_clocks.summary(),
+            note="nvidia-smi every 50 ms over the whole run (all legs), beside the timed "
+                 "region's own samples in clocks")
         print(json.dumps(line), flush=True)
+    else:
+        run_clocks.__exit__(None, None, None)
     h.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
+SPIN_CYCLES = 400_000   # about 0.2 ms of GPU spin: longer than the host takes to issue a call
+
+
 def _time_calls(fn, stream, steps, warmup, flush=None):
     """Mean device milliseconds of fn() over `steps` calls (events on `stream`), each call
     preceded by an L2 flush when `flush` (a device buffer larger than L2) is given: the buffer
-    is read, so the flush leaves no dirty lines to be written back during the timed call."""
+    is read, so the flush leaves no dirty lines to be written back during the timed call.
+    Between the flush and the start event the GPU spins for SPIN_CYCLES, so that every launch
+    of the call is queued before the start event is reached: the timed region then holds the
+    call's kernels only, not the host's time to issue them (which a single short call would
+    otherwise expose as idle GPU time)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -618,6 +713,7 @@ def _time_calls(fn, stream, steps, warmup, flush=None):
     for _ in range(steps):
         if flush is not None:
             flush.max()
+        torch.cuda._sleep(SPIN_CYCLES)
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -625,6 +721,44 @@ def _time_calls(fn, stream, steps, warmup, flush=None):
         torch.cuda.synchronize()
         total += a.elapsed_time(z)
     return total / steps
+
+
+def call_floor(dev, stream, flush) -> dict:
+    """The protocol's own floor: one tiny torch kernel timed like a verify call, with and
+    without the spin before the start event."""
+    e = torch.zeros(1, device=dev)
+    with_spin = _time_calls(lambda: e.add_(1), stream, 50, 5, flush)
+    tot = 0.0
+    for _ in range(50):
+        flush.max()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e.add_(1)
+        z.record(stream)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(z)
+    return {"tiny_kernel_us": with_spin * 1e3, "tiny_kernel_us_without_spin": tot / 50 * 1e3}
+
+
+def _kernel_split(h, fn, stream, steps, flush):
+    """Per-kernel device times of fn() (CUDA events around every launch, L2 flushed before
+    each call): {kernel class: ms per launch}."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    G.spec_profile_begin(h)
+    for _ in range(steps):
+        flush.max()
+        torch.cuda._sleep(SPIN_CYCLES)
+        fn()
+    torch.cuda.synchronize()
+    prof = G.spec_profile_end(h)
+    return {k: v[0] / v[1] for k, v in prof.items() if v[1]}
+
+
+def _hbm(bytes_moved: int, ms: float) -> dict:
+    pk, kind = peaks()
+    gbs = bytes_moved / (ms / 1e3) / 1e9
+    return {"GBps": gbs, "peak": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
+            "peak_source": kind}
 
 
 def bench_kv_commit(h, dev, stream, args):
@@ -660,15 +794,17 @@ def bench_kv_commit(h, dev, stream, args):
 
         ms = _time_calls(call, stream, 50, 5, flush)
         moved = B * (L + 1) * 2 * H * D * (2 + esz)   # read K and V, write them into the cache
-        out[name] = {"ms_per_call": ms, "bytes": moved, "GBps": moved / (ms / 1e3) / 1e9}
+        out[name] = {"ms_per_call": ms, "bytes": moved, **_hbm(moved, ms)}
     out["config"] = ("B=256 N=64, 8 slots per request, H=32 D=128 bf16 sources, NHD cache of "
                      "16-token blocks; L2 flushed before every call")
     return out
 
 
-def bench_dense_chain(dev, stream, args):
+def bench_dense_chain(dev, stream, args, check=False):
     """The dense-chain workload (B=64, k=5, V=128256, bf16 target and draft logits), one
-    spec_verify_sample call with dense draft logits; L2 flushed before every call."""
+    spec_verify_sample call with dense draft logits; L2 flushed before every call. The
+    algorithmic bytes are the target rows and the draft rows of the inner nodes (the last
+    draft row drafts nothing and is not read)."""
     from speculative_decoding_tree_mask_gb300 import binding as G
     w = W.WORKLOADS["dense_chain"]
     x = W.make(w, device=dev, seed=w.seed)
@@ -682,15 +818,32 @@ def bench_dense_chain(dev, stream, args):
                             out=out, stream=stream)
 
         ms = _time_calls(call, stream, 50, 5, flush)
+        row = w.V * x["logits"].element_size()
         moved = 2 * x["logits"].numel() * x["logits"].element_size()
-        return {"ms_per_call": ms, "value": w.B * (w.N - 1) / (ms / 1e3), "unit": UNIT,
-                "logits_bytes": moved,
-                "accept_len_mean": float(out["accept_len"].float().mean().item()),
-                "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft logits, "
-                          "T=1; L2 flushed before every call"}
+        alg = w.B * (2 * w.N - 1) * row
+        res = {"ms_per_call": ms, "value": w.B * (w.N - 1) / (ms / 1e3), "unit": UNIT,
+               "logits_bytes": moved, "algorithmic_bytes": alg,
+               "roofline": dict(_hbm(alg, ms), bound="hbm"),
+               "kernels_ms": _kernel_split(hd, call, stream, 20, flush),
+               "accept_len_mean": float(out["accept_len"].float().mean().item()),
+               "config": "dense_chain: B=64, 5 drafts, V=128256, bf16 target and draft "
+                         "logits, T=1; L2 flushed before every call"}
+        if check:
+            res["parity"] = dense_parity(x, w, snapshot(out))
+        res["protocol_floor"] = call_floor(dev, stream, flush)
+        return res
 
 
-def bench_high_accept(h, w, mask, dev, stream, args):
+def dense_parity(x, w, got: dict) -> dict:
+    from oracle import oracle as O
+    ref = O.default().verify_sample(W.host_logits(x["logits"]), x["tok_np"], x["parent_np"],
+                                    w.temperature, x["uniforms"].cpu().numpy(),
+                                    draft=W.host_logits(x["draft"]),
+                                    draft_kind=O.DRAFT_LOGITS, nthreads=os.cpu_count() or 1)
+    return parity_summary(got, ref)
+
+
+def bench_high_accept(h, w, mask, dev, stream, args, check=False):
     """The large-tree step on trees that the target mostly accepts: the same shapes with the
     grammar token boosted by 20 instead of 8 (p of a boosted child about 0.97 at T=1), so walks
     go several levels deep and a few requests reject a dominant token (the walk's full-row
@@ -718,6 +871,7 @@ def bench_high_accept(h, w, mask, dev, stream, args):
     z.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(z) / steps
+    eager_out = snapshot(out)
     G.spec_profile_begin(h)
     for _ in range(steps):
         step()
@@ -762,14 +916,20 @@ def bench_high_accept(h, w, mask, dev, stream, args):
                         (lout["out_tokens"] != out["out_tokens"]).any(dim=1).sum().item())},
            "config": f"large_tree shapes (B={wd.B} N={wd.N} V={wd.V} bf16, T=1), grammar "
                      "token boosted by 20"}
+    if check:
+        par = oracle_parity(xd, wd, {"eager_sample": ("sample", eager_out),
+                                     "lazy_sample": ("sample", snapshot(lout))},
+                            os.cpu_count() or 1)
+        res["parity"] = par["eager_sample"]
+        res["lazy"]["vs_oracle"] = par["lazy_sample"]
     del xd
     return res
 
 
-def bench_small_tries(dev, stream, args):
+def bench_small_tries(dev, stream, args, check=False):
     """The two small trie workloads (greedy: B=4, sampling: B=8; N=32, V=151936, bf16 logits),
     one verify call each; L2 flushed before every call. Their 128 and 256 rows fill less
-    than one wave of row CTAs, so each row is streamed by 4 or 2 CTAs."""
+    than one wave of row CTAs, so each row is streamed by several CTAs."""
     from speculative_decoding_tree_mask_gb300 import binding as G
     res = {}
     for name in ("greedy_trie", "sampling_trie"):
@@ -791,8 +951,14 @@ def bench_small_tries(dev, stream, args):
             moved = x["logits"].numel() * x["logits"].element_size()
             res[name] = {"ms_per_call": ms, "value": w.B * (w.N - 1) / (ms / 1e3), "unit": UNIT,
                          "logits_bytes": moved, "logit_GBps": moved / (ms / 1e3) / 1e9,
+                         "roofline": dict(_hbm(moved, ms), bound="hbm"),
+                         "kernels_ms": _kernel_split(hs, call, stream, 20, flush),
                          "config": f"{name}: B={w.B} N={w.N} V={w.V} bf16, T={w.temperature}, "
                                    "L2 flushed before every call"}
+            if check:
+                res[name]["parity"] = oracle_parity(
+                    x, w, {"call": ("greedy" if w.mode == "greedy" else "sample",
+                                    snapshot(out))}, os.cpu_count() or 1)["call"]
     return res
 
 
@@ -853,6 +1019,22 @@ def bench_budget(h, x, w, dev, stream, args):
                       "band 0.05, step 4, limits 4..64"}
 
 
+def bench_leg(args):
+    """One auxiliary leg on its own (for profiling runs): prints that leg's JSON."""
+    from speculative_decoding_tree_mask_gb300 import binding as G
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev)
+    legs = {"small_tries": lambda: bench_small_tries(dev, stream, args, not args.skip_parity),
+            "dense_chain": lambda: bench_dense_chain(dev, stream, args, not args.skip_parity)}
+    if args.leg == "kv_commit":
+        with G.Handle(256, 64, 1 << 10, 0) as h:
+            res = bench_kv_commit(h, dev, stream, args)
+    else:
+        res = legs[args.leg]()
+    print(json.dumps({"leg": args.leg, **res}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -865,12 +1047,18 @@ def main(argv=None):
     ap.add_argument("--skip-extra", action="store_true",
                     help="leave out the KV-commit and dense-chain measurements")
     ap.add_argument("--skip-lazy", action="store_true")
+    ap.add_argument("--skip-parity", action="store_true",
+                    help="leave out the comparison of every leg's outputs with the oracle")
+    ap.add_argument("--leg", choices=["small_tries", "dense_chain", "kv_commit"], default=None,
+                    help="run one auxiliary leg alone and print its JSON (profiling runs)")
     ap.add_argument("--requests", type=int, default=0,
                     help="requests per rank (default: the workload's 256); for profiling runs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.leg:
+        bench_leg(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_ours(args)

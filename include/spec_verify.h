@@ -169,7 +169,8 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
  * Here (only) logits and draft may also be page-locked host memory that the device maps at
  * the same address (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped on a
  * system with unified addressing): the visited rows are then read directly over the host
- * link, with no copy of the other rows. Other host memory returns SPEC_ERR_ARG.
+ * link, with no copy of the other rows. Other host memory, and device memory of a GPU other
+ * than the handle's, return SPEC_ERR_ARG (checked with cudaPointerGetAttributes).
  */
 int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B, int N,
                             int64_t V, const int32_t *draft_token, const int32_t *parent,
@@ -305,11 +306,17 @@ const char *spec_error_string(int code);
  * the current device, and the per-row scratch (argmax and flags of each of the B*N rows) is
  * a static device array of SPEC_NOALLOC_MAX_ROWS rows (128 KiB) that every GPU loading the
  * library holds until the process exits. B*N > SPEC_NOALLOC_MAX_ROWS returns SPEC_ERR_ARG
- * and launches nothing. No cudaMalloc, cudaFree or allocating library call is made.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * once; make that first call before any stream capture. All calls share the one array
- * (each call writes every row it reads, so stale contents do not matter), so calls that
- * overlap on the GPU, on any streams, race: serialise them.
+ * and launches nothing, and so do logits that are not memory of the current device
+ * (checked with cudaPointerGetAttributes). No cudaMalloc, cudaFree or allocating library
+ * call is made.
+ * The first call in a CUDA context looks up the array's device address in that context
+ * (cudaGetSymbolAddress) and caches it with the context's ID; make that first call before
+ * any stream capture. A new context on the device (after cudaDeviceReset, or another
+ * driver-API context made current) loads the library's module at a new address: the next
+ * call sees the new context ID and looks the address up again, so it too should come before
+ * any capture. All calls share the one array (each call writes every row it reads, so stale
+ * contents do not matter), so calls that overlap on the GPU, on any streams, race:
+ * serialise them.
  */
 #define SPEC_NOALLOC_MAX_ROWS 16384
 int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, int N, int64_t V,

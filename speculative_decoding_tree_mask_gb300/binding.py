@@ -113,6 +113,19 @@ def _ptr_dev_or_pinned(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _hdev(h) -> str:
+    return f"cuda:{h.device}"
+
+
+def _same_device(tensors, device, where):
+    """Every CUDA tensor of a call must live on `device` (the handle's GPU, or for the
+    handle-free call the logits' GPU): the kernels run there and take raw addresses."""
+    dev = torch.device(device)
+    for t in tensors:
+        if t is not None and t.is_cuda and t.device != dev:
+            raise ValueError(f"{where}: a tensor is on {t.device}, the call runs on {dev}")
+
+
 def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -174,6 +187,7 @@ def spec_build_tree_mask(h: Handle, parent, anc_mask, depth, status, stream=None
     """parent int32 [B, N] -> anc_mask int64 [B, N] (uint64 bit patterns), depth int32 [B, N],
     status int32 [B]."""
     B, N = parent.shape
+    _same_device((parent, anc_mask, depth, status), _hdev(h), "spec_build_tree_mask")
     if anc_mask.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)):
         raise TypeError("anc_mask must be a 64-bit integer tensor")
     _check(load().spec_build_tree_mask(h.ptr, _ptr(_i32(parent, "parent")), B, N, _ptr(anc_mask),
@@ -184,6 +198,8 @@ def spec_build_tree_mask(h: Handle, parent, anc_mask, depth, status, stream=None
 def spec_verify_greedy(h: Handle, logits, draft_token, parent, accept_len, out_tokens, kv_commit,
                        bonus, status, stream=None):
     B, N, V = logits.shape
+    _same_device((logits, draft_token, parent, accept_len, out_tokens, kv_commit, bonus, status),
+                 _hdev(h), "spec_verify_greedy")
     _check(load().spec_verify_greedy(
         h.ptr, _ptr(logits), _dtype_code(logits), B, N, V,
         _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
@@ -195,6 +211,8 @@ def spec_verify_sample(h: Handle, logits, draft_token, parent, temperature: floa
                        accept_len, out_tokens, kv_commit, bonus, status, draft=None,
                        draft_kind: int = SPEC_DRAFT_POINT, stream=None):
     B, N, V = logits.shape
+    _same_device((logits, draft_token, parent, uniforms, accept_len, out_tokens, kv_commit,
+                  bonus, status, draft), _hdev(h), "spec_verify_sample")
     ddt = 0
     if draft is not None and draft_kind == SPEC_DRAFT_LOGITS:
         ddt = _dtype_code(draft)
@@ -212,6 +230,8 @@ def spec_verify_greedy_lazy(h: Handle, logits, draft_token, parent, accept_len, 
                             kv_commit, bonus, status, stream=None):
     """Greedy verification reading only the rows on the accepted path."""
     B, N, V = logits.shape
+    _same_device((logits, draft_token, parent, accept_len, out_tokens, kv_commit, bonus, status),
+                 _hdev(h), "spec_verify_greedy_lazy")
     _check(load().spec_verify_greedy_lazy(
         h.ptr, _ptr_dev_or_pinned(logits), _dtype_code(logits), B, N, V,
         _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
@@ -224,6 +244,8 @@ def spec_verify_sample_lazy(h: Handle, logits, draft_token, parent, temperature:
                             draft_kind: int = SPEC_DRAFT_POINT, stream=None):
     """Sampling verification reading only the rows the walk visits."""
     B, N, V = logits.shape
+    _same_device((logits, draft_token, parent, uniforms, accept_len, out_tokens, kv_commit,
+                  bonus, status, draft), _hdev(h), "spec_verify_sample_lazy")
     ddt = 0
     if draft is not None and draft_kind == SPEC_DRAFT_LOGITS:
         ddt = _dtype_code(draft)
@@ -243,6 +265,8 @@ def spec_row_stats(h: Handle, logits, N: int, temperature: float, row_max, row_s
     p_parent(token) at every child into child_prob [B, N]."""
     V = logits.shape[-1]
     rows = logits.numel() // V
+    _same_device((logits, row_max, row_sum, row_argmax, row_flags, draft_token, parent,
+                  child_prob), _hdev(h), "spec_row_stats")
     _check(load().spec_row_stats(
         h.ptr, _ptr(logits), _dtype_code(logits), rows, int(N), V, float(temperature),
         _ptr(draft_token), _ptr(parent), _ptr(row_max), _ptr(row_sum), _ptr(row_argmax),
@@ -262,6 +286,8 @@ def spec_kv_commit(h: Handle, src_k, src_v, kv_commit, accept_len, cache_k, cach
     (NHD [blocks, block_size, H, D] or HND [blocks, H, block_size, D]); fp8 caches are uint8.
     Scales: float32 tensors of one element, or [B, N] (one per source token)."""
     B, N, H, D = src_k.shape
+    _same_device((src_k, src_v, kv_commit, accept_len, cache_k, cache_v, block_table, seq_pos,
+                  k_scale, v_scale, commit_status), _hdev(h), "spec_kv_commit")
     if layout == SPEC_KV_NHD:
         num_blocks, block_size = cache_k.shape[0], cache_k.shape[1]
     else:
@@ -297,6 +323,7 @@ def spec_budget_update(h: Handle, params: BudgetParams, accept_len, status, pare
                        n_active, stream=None):
     """One controller update on the device; ``state`` is a tensor from budget_state()."""
     B, N = parent.shape
+    _same_device((accept_len, status, parent, state, n_active), _hdev(h), "spec_budget_update")
     if state.dtype != torch.float64 or state.numel() != 2:
         raise TypeError("state must be the float64 [2] tensor made by budget_state()")
     _check(load().spec_budget_update(
@@ -407,7 +434,12 @@ def spec_verify_greedy_noalloc(logits, draft_token, parent, accept_len, out_toke
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         fn.argtypes = [P, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
     B, N, V = logits.shape
-    _check(fn(_ptr(logits), _dtype_code(logits), B, N, V, _ptr(_i32(draft_token, "draft_token")),
-              _ptr(_i32(parent, "parent")), _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit),
-              _ptr(bonus), _ptr(status), _stream(stream, logits.device)),
-           "spec_verify_greedy_noalloc")
+    tensors = (logits, draft_token, parent, accept_len, out_tokens, kv_commit, bonus, status)
+    _same_device(tensors, logits.device, "spec_verify_greedy_noalloc")
+    # the library runs on the current device: make it the tensors' device for the call
+    with torch.cuda.device(logits.device):
+        _check(fn(_ptr(logits), _dtype_code(logits), B, N, V,
+                  _ptr(_i32(draft_token, "draft_token")), _ptr(_i32(parent, "parent")),
+                  _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus),
+                  _ptr(status), _stream(stream, logits.device)),
+               "spec_verify_greedy_noalloc")

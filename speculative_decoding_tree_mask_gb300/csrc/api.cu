@@ -96,16 +96,18 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
 
-// Lazy calls read logits where they live: device memory, or page-locked host memory that
-// the device reaches at the same address (read over the host link). Anything else (pageable
-// host memory, a registration mapped at another address) is refused.
-bool readable_by_device(const void *p) {
+// Lazy calls read logits where they live: memory of the handle's device, or page-locked
+// host memory that the device reaches at the same address (read over the host link).
+// Anything else (another GPU's memory, pageable host memory, a registration mapped at
+// another address) is refused.
+bool readable_by_device(const void *p, int device) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+    if (a.type == cudaMemoryTypeDevice) return a.device == device;
+    if (a.type == cudaMemoryTypeManaged) return true;
     return a.type == cudaMemoryTypeHost && a.devicePointer == p;
 }
 
@@ -428,7 +430,7 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
     if (rc != SPEC_OK || B == 0) return rc;
     DeviceScope ds(h->device);
     if (!ds.ok()) return SPEC_ERR_CUDA;
-    if (!readable_by_device(logits)) return SPEC_ERR_ARG;
+    if (!readable_by_device(logits, h->device)) return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     LazyGreedyParams lp;
     lp.B = B;
@@ -472,7 +474,9 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
     }
     DeviceScope ds(h->device);
     if (!ds.ok()) return SPEC_ERR_CUDA;
-    if (!readable_by_device(logits) || (draft && !readable_by_device(draft))) return SPEC_ERR_ARG;
+    if (!readable_by_device(logits, h->device) ||
+        (draft && !readable_by_device(draft, h->device)))
+        return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     SampleWalkParams wp{};
     wp.B = B;
@@ -593,6 +597,7 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
     kp.v_scale = v_scale;
     kp.scale_per_token = scale_per_token;
     kp.status = commit_status;
+    kp.sms = h->sms;
     // 8 elements per thread step: rows of D elements and 16-byte aligned bases.
     const bool vec = D % 8 == 0 && aligned(src_k, 16) && aligned(src_v, 16) &&
                      aligned(cache_k, 16) && aligned(cache_v, 16);

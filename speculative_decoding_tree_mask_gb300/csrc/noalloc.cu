@@ -8,6 +8,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "spec_internal.h"
 #include "spec_verify.h"
 
@@ -20,30 +22,88 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[2 * SPEC_NOALLOC_MAX_
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-int32_t *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device. In host code the array's name
-// is only a host-side stand-in, so the address is looked up once per device (with that
-// device current) and cached.
-int scratch_address(int32_t **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+// The array's address belongs to the context the module was loaded in: after
+// cudaDeviceReset, or under another driver-API context made current on the same device, the
+// module is loaded again at another address. So the cached address is kept per device
+// together with the ID of the context it was looked up in, and looked up again whenever the
+// current context's ID differs.
+struct ScratchEntry {
+    unsigned long long ctx = 0;
+    int32_t *addr = nullptr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxDevices];
+
+// Driver calls that read the current context's ID, resolved through the runtime (so the
+// library needs no link-time dependency on the driver library).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+bool resolve_driver_calls() {
+    if (g_ctx_get_current && g_ctx_get_id) return true;
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) !=
+            cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+            cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !a || !b) {
+        cudaGetLastError();
+        return false;
+    }
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+    return true;
+}
+
+// ID of the current context; false when no context is current yet.
+bool current_context_id(unsigned long long *id) {
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context of device `dev`. In host code
+// the array's name is only a host-side stand-in, so the address is looked up with that
+// context current (cudaGetSymbolAddress) and cached with the context's ID.
+int scratch_address(int dev, int32_t **out) {
+    if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!resolve_driver_calls()) return SPEC_ERR_CUDA;
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    ScratchEntry &e = g_scratch[dev];
+    if (have_id && e.addr != nullptr && e.ctx == id) {
+        *out = e.addr;
+        return SPEC_OK;
+    }
+    // Looking the symbol up also makes the runtime's context current if none was yet.
+    void *p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
     }
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return SPEC_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = static_cast<int32_t *>(p);
-    }
-    *out = g_scratch_addr[dev];
+    if (!have_id && !current_context_id(&id)) return SPEC_ERR_CUDA;
+    e.ctx = id;
+    e.addr = static_cast<int32_t *>(p);
+    *out = e.addr;
     return SPEC_OK;
+}
+
+// The logits must be memory of the current device (they are streamed by the row-statistics
+// kernel, launched there): device memory of another GPU is refused rather than read
+// through an address that is not valid on this one.
+bool on_device(const void *p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
 }
 
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -67,8 +127,14 @@ extern "C" int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, 
     for (const void *p : ints)
         if (!aligned_to(p, 4)) return SPEC_ERR_ARG;
 
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+    if (!on_device(logits, dev)) return SPEC_ERR_ARG;
     int32_t *scratch = nullptr;
-    const int rc = scratch_address(&scratch);
+    const int rc = scratch_address(dev, &scratch);
     if (rc != SPEC_OK) return rc;
     int32_t *arg = scratch;
     int32_t *flags = scratch + SPEC_NOALLOC_MAX_ROWS;

@@ -201,6 +201,7 @@ struct KvCommitParams {
     const float *k_scale, *v_scale;
     int scale_per_token;          // 1: scales are [B, N], per source token
     int32_t *status;
+    int sms;                      // SMs of the device (the grid is a few CTAs per SM)
 };
 
 cudaError_t launch_kv_commit(const KvCommitParams &p, bool vec, cudaStream_t st);

@@ -14,24 +14,38 @@ from speculative_decoding_tree_mask_gb300 import workloads as W
 
 def test_clock_summary_median_max_and_reasons():
     s = bench.ClockSampler(0)
-    s.lines = [
+    s.lines = [(float(i), ln) for i, ln in enumerate([
         "2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
         "1980, 2070, 1210.0, 0x4, Not Active, Not Active, Not Active, Active",
         "2070, 2070, 1300.2, 0x0, Not Active, Not Active, Not Active, Not Active",
         "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",   # unreadable
         "garbage",
-    ]
+    ])]
     out = s.summary()
     assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
     assert out["samples"] == 3
     assert out["reasons"] == ["sw_power_cap"]
-    s.lines.append("1400, 2070, 1390, 0x8, Active, Not Active, Active, Not Active")
+    s.lines.append((5.0, "1400, 2070, 1390, 0x8, Active, Not Active, Active, Not Active"))
     assert s.summary()["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_of_a_short_region_takes_the_bracketing_samples():
+    """A timed region shorter than the sampling interval still gets the samples on both
+    sides of it (within one interval); samples farther away are left out."""
+    s = bench.ClockSampler(0, interval_ms=50)
+    row = "{}, 2070, 1000, 0x0, Not Active, Not Active, Not Active, {}"
+    s.lines = [(0.90, row.format(1000, "Active")), (0.98, row.format(2070, "Not Active")),
+               (1.03, row.format(2060, "Not Active")), (1.20, row.format(1500, "Active"))]
+    s.mark(1.00, 1.014)
+    out = s.summary(region=True)
+    assert out["samples"] == 2 and out["sm_mhz"] == 2065.0 and out["reasons"] == []
+    assert s.summary()["samples"] == 4 and s.summary()["reasons"] == ["sw_power_cap"]
 
 
 def test_clock_summary_without_samples():
     out = bench.ClockSampler(0).summary()
-    assert out == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    assert out == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                   "interval_ms": 50}
 
 
 def _copy_tree(tmp_path):

@@ -127,4 +127,4 @@ def test_fuzz_against_oracle(h, orc, seed):
     if c["mode"] == "greedy":
         PY.assert_exact(got, ref)
     else:
-        PY.compare_sample(got, ref, max_excluded_frac=0.25)
+        PY.compare_sample(got, ref)

@@ -4,6 +4,7 @@ Greedy results, masks and argmax are compared bit for bit; sampling results are 
 except requests whose oracle decision or inverse-CDF margin is below 1e-6 (counted).
 """
 import itertools
+import os
 
 import numpy as np
 import pytest
@@ -432,17 +433,14 @@ def test_large_tree_full_size(h, orc):
         assert (gpu["out_tokens"][b, :L] == tok[kv[1:L + 1]]).all()
         kids = [c for c in range(w.N) if par[c] == kv[L]]
         assert gpu["bonus"][b] not in tok[kids]       # rejected tokens leave the residual
-    # a sample of requests against the oracle
-    rows = np.r_[0:8, np.random.default_rng(0).choice(np.arange(8, w.B), 8, replace=False)]
-    ridx = torch.as_tensor(rows, device=DEV)
-    ref = PY.oracle_sample(orc, x["logits"][ridx], x["draft_token"][ridx], x["parent"][ridx], T,
-                           x["uniforms"][ridx])
-    PY.compare_sample(gpu, ref, rows=rows)
-    # greedy on the same sample
+    # every request against the oracle: sampling, then greedy on the same trees
+    threads = os.cpu_count() or 8
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], T, x["uniforms"],
+                           nthreads=threads)
+    PY.compare_sample(gpu, ref)
     gg = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
-    gref = orc.verify_greedy(PY.host(x["logits"][ridx]), x["tok_np"][rows], x["parent_np"][rows],
-                             nthreads=8)
-    PY.assert_exact(gg, gref, rows=rows)
+    gref = orc.verify_greedy(PY.host(x["logits"]), x["tok_np"], x["parent_np"], nthreads=threads)
+    PY.assert_exact(gg, gref)
 
 
 # ---- losslessness on the GPU (Monte Carlo against the exact law) --------------------------------
