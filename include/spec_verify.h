@@ -70,8 +70,13 @@ enum {
                                    (for probabilities: NaN, inf or a negative entry) */
     SPEC_REQ_BAD_UNIFORM = 4,   /* a uniform in slots 1..N is NaN or outside [0, 1) */
     SPEC_REQ_BAD_SLOT = 5,      /* KV commit: a slot maps outside the block table or cache */
-    SPEC_REQ_BAD_BUDGET = 6     /* the request's node budget (spec_set_node_budget) is
+    SPEC_REQ_BAD_BUDGET = 6,    /* the request's node budget (spec_set_node_budget) is
                                    outside [1, N] */
+    SPEC_REQ_INTERNAL = 7       /* debug builds only (SPEC_DEBUG): one of the kernels' own
+                                   consistency checks failed for this request -- an index
+                                   outside its array (the access was skipped), a split row's
+                                   arrival counter outside [0, split), or an accepted path that
+                                   is not a chain of parent links; see spec_debug_words */
 };
 
 enum { SPEC_KV_NHD = 0, SPEC_KV_HND = 1 };  /* paged KV cache layouts */
@@ -97,8 +102,8 @@ enum {
 
 /*
  * Create a handle for `device` able to serve calls with B <= max_B, N <= max_N (<= 64) and
- * V <= max_V (<= 2^21). Allocates a device workspace of 232 * max_B * max_N bytes with
- * cudaMalloc (released by spec_verify_destroy). Returns SPEC_ERR_ARG for out-of-range limits,
+ * V <= max_V (<= 2^21). Allocates a device workspace of 232 * max_B * max_N + 4 * max_B
+ * bytes with cudaMalloc (released by spec_verify_destroy). Returns SPEC_ERR_ARG for out-of-range limits,
  * SPEC_ERR_CUDA if the device cannot be used, SPEC_ERR_WORKSPACE if allocation fails.
  */
 int spec_verify_init(spec_handle *h, int max_B, int max_N, int64_t max_V, int device);
@@ -295,6 +300,32 @@ int spec_budget_update(spec_handle h, const spec_budget_params *params,
 
 /* Static description of a SPEC_ERR_* code. */
 const char *spec_error_string(int code);
+
+/*
+ * Debug flavour. The library built with SPEC_DEBUG (libspecverify_debug.so) runs the same
+ * kernels with their own consistency checks compiled in: every vector index of the vocabulary
+ * streams, every store into the walks' shared arrays, the accepted path (a chain of parent
+ * links from the root), the bonus token (in [0, V), not a rejected token), the KV commit's
+ * source and cache indices, and the split rows' arrival counters (each arrival must see a
+ * value in [0, split)). A failed check skips the access, sets a bit in the request's debug
+ * word (1 index, 2 arrival counter, 4 walk) and turns the request's result into
+ * SPEC_REQ_INTERNAL (the KV commit's status likewise). Nothing traps or waits. Each verify
+ * call of the debug build first zeroes the debug words of its requests and all arrival
+ * counters. The EmbodiInfer PR #11 commit e9133f4 lesson (stale NaN slots must not reach an
+ * output) and the TensorRT-LLM PR #16953 debug-flagged checks motivate this flavour.
+ *
+ * spec_debug_build: 1 in the debug build, 0 otherwise.
+ * spec_debug_inject_arrival: arms a one-shot fault injection for tests: the next verify call
+ *   on the handle whose row statistics are split over several CTAs per row writes `value`
+ *   into the arrival counter of row `row` (b * N + node) after zeroing the counters, so its
+ *   check must catch it. Returns SPEC_ERR_UNSUPPORTED in release builds.
+ * spec_debug_words: copies the debug words of requests 0..B-1 of the handle's last call into
+ *   the device int32 array `words` (asynchronously on `stream`). SPEC_ERR_UNSUPPORTED in
+ *   release builds.
+ */
+int spec_debug_build(void);
+int spec_debug_inject_arrival(spec_handle h, int row, int value);
+int spec_debug_words(spec_handle h, int32_t *words, int B, void *stream);
 
 /*
  * Greedy verification that allocates nothing. The pages have no counterpart of this entry

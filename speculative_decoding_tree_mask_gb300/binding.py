@@ -6,6 +6,7 @@ Loading fails loudly when the library has not been built.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -14,6 +15,7 @@ import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(HERE, "libspecverify.so")
+DEBUG_LIBRARY = os.path.join(HERE, "libspecverify_debug.so")   # checked flavour (SPEC_DEBUG)
 
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE = 0, -1, -2, -3, -4
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -26,6 +28,8 @@ KERNEL_CLASSES = ("tree_mask", "row_stats", "draft_stats", "walk_greedy", "walk_
 SPEC_F16 = 2
 SPEC_REQ_BAD_SLOT = 5
 SPEC_REQ_BAD_BUDGET = 6
+SPEC_REQ_INTERNAL = 7   # debug builds: a kernel's own consistency check failed
+DBG_INDEX, DBG_ARRIVAL, DBG_WALK = 1, 2, 4
 SPEC_KV_NHD, SPEC_KV_HND = 0, 1
 SPEC_CACHE_SAME, SPEC_CACHE_FP8_E4M3, SPEC_CACHE_FP8_E5M2 = 0, 1, 2
 SPEC_SCALE_TENSOR, SPEC_SCALE_PER_TOKEN = 0, 1
@@ -54,32 +58,56 @@ def load() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIBRARY):
-                raise RuntimeError(
-                    f"{LIBRARY} is missing: build it first "
-                    "(python -m speculative_decoding_tree_mask_gb300.build)")
-            lib = ctypes.CDLL(LIBRARY)
-            P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
-            lib.spec_verify_init.argtypes = [ctypes.POINTER(P), i32, i32, i64, i32]
-            lib.spec_verify_destroy.argtypes = [P]
-            lib.spec_build_tree_mask.argtypes = [P, P, i32, i32, P, P, P, P]
-            lib.spec_verify_greedy.argtypes = [P, P, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
-            lib.spec_verify_sample.argtypes = [P, P, i32, i32, i32, i64, P, P, P, i32, i32, f32,
-                                               P, P, P, P, P, P, P]
-            lib.spec_row_stats.argtypes = [P, P, i32, i32, i32, i64, f32, P, P, P, P, P, P, P, P]
-            lib.spec_verify_greedy_lazy.argtypes = lib.spec_verify_greedy.argtypes
-            lib.spec_kv_commit.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32,
-                                           i32, i32, i64, P, i32, P, P, P, i32, P, P]
-            lib.spec_verify_sample_lazy.argtypes = lib.spec_verify_sample.argtypes
-            lib.spec_set_node_budget.argtypes = [P, P]
-            lib.spec_budget_update.argtypes = [P, ctypes.POINTER(BudgetParams), P, P, P, i32,
-                                               i32, P, P, P]
-            lib.spec_profile_begin.argtypes = [P]
-            lib.spec_profile_end.argtypes = [P, P, P]
-            lib.spec_error_string.argtypes = [i32]
-            lib.spec_error_string.restype = ctypes.c_char_p
-            _lib = lib
+            _lib = _open(LIBRARY)
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call of this module through another build of the library (for example the
+    debug flavour, DEBUG_LIBRARY) inside the `with` block. Handles are tied to the build that
+    created them: make them inside the block."""
+    global _lib
+    lib = _open(path)
+    with _lock:
+        prev = _lib
+        _lib = lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first "
+            "(python -m speculative_decoding_tree_mask_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.spec_verify_init.argtypes = [ctypes.POINTER(P), i32, i32, i64, i32]
+    lib.spec_verify_destroy.argtypes = [P]
+    lib.spec_build_tree_mask.argtypes = [P, P, i32, i32, P, P, P, P]
+    lib.spec_verify_greedy.argtypes = [P, P, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+    lib.spec_verify_sample.argtypes = [P, P, i32, i32, i32, i64, P, P, P, i32, i32, f32,
+                                       P, P, P, P, P, P, P]
+    lib.spec_row_stats.argtypes = [P, P, i32, i32, i32, i64, f32, P, P, P, P, P, P, P, P]
+    lib.spec_verify_greedy_lazy.argtypes = lib.spec_verify_greedy.argtypes
+    lib.spec_kv_commit.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, i32,
+                                   i32, i32, i64, P, i32, P, P, P, i32, P, P]
+    lib.spec_verify_sample_lazy.argtypes = lib.spec_verify_sample.argtypes
+    lib.spec_set_node_budget.argtypes = [P, P]
+    lib.spec_budget_update.argtypes = [P, ctypes.POINTER(BudgetParams), P, P, P, i32,
+                                       i32, P, P, P]
+    lib.spec_profile_begin.argtypes = [P]
+    lib.spec_profile_end.argtypes = [P, P, P]
+    lib.spec_error_string.argtypes = [i32]
+    lib.spec_error_string.restype = ctypes.c_char_p
+    lib.spec_debug_build.argtypes = []
+    lib.spec_debug_inject_arrival.argtypes = [P, i32, i32]
+    lib.spec_debug_words.argtypes = [P, P, i32, P]
+    return lib
 
 
 def error_string(code: int) -> str:
@@ -443,3 +471,25 @@ def spec_verify_greedy_noalloc(logits, draft_token, parent, accept_len, out_toke
                   _ptr(accept_len), _ptr(out_tokens), _ptr(kv_commit), _ptr(bonus),
                   _ptr(status), _stream(stream, logits.device)),
                "spec_verify_greedy_noalloc")
+
+
+# ---- debug flavour -------------------------------------------------------------------------
+
+def spec_debug_build() -> bool:
+    """True when the loaded library is the checked (SPEC_DEBUG) build."""
+    return bool(load().spec_debug_build())
+
+
+def spec_debug_inject_arrival(h: Handle, row: int, value: int):
+    """Debug builds: the next split row-statistics launch on ``h`` finds ``value`` in the
+    arrival counter of ``row`` (a test of the counter check)."""
+    _check(load().spec_debug_inject_arrival(h.ptr, int(row), int(value)),
+           "spec_debug_inject_arrival")
+
+
+def spec_debug_words(h: Handle, B: int, stream=None) -> torch.Tensor:
+    """Debug builds: the violation bits (DBG_*) of requests 0..B-1 in the handle's last call."""
+    words = torch.empty(B, dtype=torch.int32, device=_hdev(h))
+    _check(load().spec_debug_words(h.ptr, _ptr(words), int(B), _stream(stream, words.device)),
+           "spec_debug_words")
+    return words

@@ -49,7 +49,9 @@ struct spec_ctx {
     float2 *chunk = nullptr;              // row-chunk partials of the target rows
     RowPart *piece = nullptr;             // small batches: per-piece row statistics
     int32_t *count = nullptr;             // ... and per-row arrivals (zero between calls)
-    int slots = 0;                        // CTAs of the row-statistics kernel in one wave
+    int32_t *dbg = nullptr;               // debug builds: violation bits per request [max_B]
+    int inject_row = -1, inject_value = 0;   // debug builds: one armed counter injection
+    int slots = 0;                        // CTAs of the split row-statistics kernel in a wave
     int sms = 0;                          // streaming multiprocessors of the device
     const int32_t *n_active = nullptr;   // node budget set by spec_set_node_budget
     bool prof = false;
@@ -157,6 +159,31 @@ int walk_cluster(spec_handle h, int B, bool point) {
     return 1;
 }
 
+// Debug builds, before a verify call's kernels: zero the request's violation words and every
+// split-row arrival counter (so a counter an earlier call left wrong cannot spill over), then
+// apply an injection armed by spec_debug_inject_arrival. Release builds do nothing.
+int debug_prologue(spec_handle h, int B, int rows, cudaStream_t st) {
+#ifdef SPEC_DEBUG
+    const int64_t cap = (int64_t)h->max_B * h->max_N;
+    if (cudaMemsetAsync(h->dbg, 0, sizeof(int32_t) * (size_t)B, st) != cudaSuccess ||
+        cudaMemsetAsync(h->count, 0, sizeof(int32_t) * (size_t)cap, st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (h->inject_row >= 0 && h->inject_row < rows && h->inject_row < cap) {
+        if (cudaMemcpyAsync(h->count + h->inject_row, &h->inject_value, sizeof(int32_t),
+                            cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return SPEC_ERR_CUDA;
+        h->inject_row = -1;
+    }
+#else
+    (void)h;
+    (void)B;
+    (void)rows;
+    (void)st;
+#endif
+    return SPEC_OK;
+}
+
 WalkOutputs outputs(int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit,
                     int32_t *bonus, int32_t *status) {
     WalkOutputs o;
@@ -170,6 +197,8 @@ WalkOutputs outputs(int32_t *accept_len, int32_t *out_tokens, int32_t *kv_commit
 
 int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int64_t V,
                 const int32_t *tok, const int32_t *parent, WalkOutputs out, cudaStream_t st) {
+    const int drc = debug_prologue(h, B, B * N, st);
+    if (drc != SPEC_OK) return drc;
     RowStatsParams rp{};
     rp.x = logits;
     rp.V = V;
@@ -181,6 +210,7 @@ int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int6
     rp.arg = h->arg;
     rp.flags = h->flags;
     rp.n_active = h->n_active;
+    rp.dbg = h->dbg;
     set_split(h, rp);
     int rc = timed(h, SPEC_K_ROW_STATS, st,
                    [&] { return launch_row_stats(rp, dtype, ROW_GREEDY, st); });
@@ -195,6 +225,7 @@ int greedy_impl(spec_handle h, const void *logits, int dtype, int B, int N, int6
     gp.flags = h->flags;
     gp.out = out;
     gp.n_active = h->n_active;
+    gp.dbg = h->dbg;
     return timed(h, SPEC_K_WALK_GREEDY, st, [&] { return launch_walk_greedy(gp, st); });
 }
 
@@ -233,7 +264,8 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
     h->max_V = max_V;
     const size_t rows = (size_t)max_B * max_N;
     const size_t bytes =
-        rows * (9 * 4 + kRowChunks * sizeof(float2) + kRowChunks * sizeof(RowPart) + 4);
+        rows * (9 * 4 + kRowChunks * sizeof(float2) + kRowChunks * sizeof(RowPart) + 4) +
+        sizeof(int32_t) * (size_t)max_B;
     if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
         cudaGetLastError();
         delete h;
@@ -257,15 +289,17 @@ int spec_verify_init(spec_handle *out, int max_B, int max_N, int64_t max_V, int 
     h->flags = reinterpret_cast<int32_t *>(take(rows * 4));
     h->dflags = reinterpret_cast<int32_t *>(take(rows * 4));
     h->count = reinterpret_cast<int32_t *>(take(rows * 4));
+    h->dbg = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * (size_t)max_B));
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaMemset(h->count, 0, rows * 4) != cudaSuccess) {
+        cudaMemset(h->count, 0, rows * 4) != cudaSuccess ||
+        cudaMemset(h->dbg, 0, sizeof(int32_t) * (size_t)max_B) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(h->ws);
         delete h;
         return SPEC_ERR_CUDA;
     }
-    h->slots = 6 * sms;   // the row-statistics kernel keeps 6 CTAs on every SM
+    h->slots = kSplitCtasPerSm * sms;   // one wave of the split row-statistics kernel
     h->sms = sms;
     *out = h;
     return SPEC_OK;
@@ -345,6 +379,8 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
         const size_t de = draft_kind == SPEC_DRAFT_LOGITS ? esize(draft_dtype) : 4;
         if (!aligned(draft, de)) return SPEC_ERR_ARG;
     }
+    rc = debug_prologue(h, B, B * N, st);
+    if (rc != SPEC_OK) return rc;
 
     RowStatsParams rp{};
     rp.x = logits;
@@ -363,6 +399,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     rp.pc = h->pc;
     rp.n_active = h->n_active;
     rp.chunk = h->chunk;
+    rp.dbg = h->dbg;
     if (!dense) {
         set_split(h, rp);
         rc = timed(h, SPEC_K_ROW_STATS, st,
@@ -417,6 +454,7 @@ int spec_verify_sample(spec_handle h, const void *logits, int dtype, int B, int 
     wp.n_active = h->n_active;
     wp.chunk = draft_kind == SPEC_DRAFT_POINT ? h->chunk : nullptr;
     wp.cluster = walk_cluster(h, B, draft_kind == SPEC_DRAFT_POINT);
+    wp.dbg = h->dbg;
     return timed(h, SPEC_K_WALK_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
 }
 
@@ -432,6 +470,8 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
     if (!ds.ok()) return SPEC_ERR_CUDA;
     if (!readable_by_device(logits, h->device)) return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = debug_prologue(h, B, 0, st);
+    if (rc != SPEC_OK) return rc;
     LazyGreedyParams lp;
     lp.B = B;
     lp.N = N;
@@ -442,6 +482,7 @@ int spec_verify_greedy_lazy(spec_handle h, const void *logits, int dtype, int B,
     lp.tok = draft_token;
     lp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
     lp.n_active = h->n_active;
+    lp.dbg = h->dbg;
     return timed(h, SPEC_K_LAZY_GREEDY, st, [&] { return launch_lazy_greedy(lp, st); });
 }
 
@@ -478,6 +519,8 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
         (draft && !readable_by_device(draft, h->device)))
         return SPEC_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = debug_prologue(h, B, 0, st);
+    if (rc != SPEC_OK) return rc;
     SampleWalkParams wp{};
     wp.B = B;
     wp.N = N;
@@ -494,6 +537,7 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
     wp.lazy = 1;
     wp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
     wp.n_active = h->n_active;
+    wp.dbg = h->dbg;
     return timed(h, SPEC_K_LAZY_SAMPLE, st, [&] { return launch_walk_sample(wp, st); });
 }
 
@@ -601,6 +645,12 @@ int spec_kv_commit(spec_handle h, const void *src_k, const void *src_v, int src_
     // 8 elements per thread step: rows of D elements and 16-byte aligned bases.
     const bool vec = D % 8 == 0 && aligned(src_k, 16) && aligned(src_v, 16) &&
                      aligned(cache_k, 16) && aligned(cache_v, 16);
+#ifdef SPEC_DEBUG
+    // debug builds combine statuses with atomicMax, from zero
+    if (commit_status &&
+        cudaMemsetAsync(commit_status, 0, sizeof(int32_t) * (size_t)B, st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+#endif
     return timed(h, SPEC_K_KV_COMMIT, st, [&] { return launch_kv_commit(kp, vec, st); });
 }
 
@@ -639,6 +689,10 @@ int spec_row_stats(spec_handle h, const void *logits, int dtype, int rows, int N
     rp.flags = row_flags;
     rp.pc = gather ? child_prob : nullptr;
     set_split(h, rp);
+    if (rp.split > 1) {
+        const int drc = debug_prologue(h, 0, rows, st);
+        if (drc != SPEC_OK) return drc;
+    }
     const int mode = temperature > 0.f ? ROW_SAMPLE : ROW_GREEDY;
     return timed(h, SPEC_K_ROW_STATS, st, [&] { return launch_row_stats(rp, dtype, mode, st); });
 }
@@ -679,6 +733,50 @@ int spec_profile_end(spec_handle h, float *ms_per_class, int32_t *launches_per_c
     h->prof = false;
     h->nrec = 0;
     return rc;
+}
+
+int spec_debug_build(void) {
+    SPEC_RANGE("spec_debug_build");
+#ifdef SPEC_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int spec_debug_inject_arrival(spec_handle h, int row, int value) {
+    SPEC_RANGE("spec_debug_inject_arrival");
+#ifdef SPEC_DEBUG
+    if (!h || row < 0 || (int64_t)row >= (int64_t)h->max_B * h->max_N) return SPEC_ERR_ARG;
+    h->inject_row = row;
+    h->inject_value = value;
+    return SPEC_OK;
+#else
+    (void)h;
+    (void)row;
+    (void)value;
+    return SPEC_ERR_UNSUPPORTED;
+#endif
+}
+
+int spec_debug_words(spec_handle h, int32_t *words, int B, void *stream) {
+    SPEC_RANGE("spec_debug_words");
+#ifdef SPEC_DEBUG
+    if (!h || B < 0 || B > h->max_B || (B > 0 && !words)) return SPEC_ERR_ARG;
+    if (B == 0) return SPEC_OK;
+    DeviceScope ds(h->device);
+    if (!ds.ok()) return SPEC_ERR_CUDA;
+    return cudaMemcpyAsync(words, h->dbg, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToDevice,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SPEC_OK
+               : SPEC_ERR_CUDA;
+#else
+    (void)h;
+    (void)words;
+    (void)B;
+    (void)stream;
+    return SPEC_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -20,6 +20,7 @@ constexpr int kWarps = kThreads / 32;
 struct LazySmem {
     int par[kMaxN], tok[kMaxN], path[kMaxN];
     int st, next;
+    int dbgv;   // debug builds: violation bits found by this CTA
     rowpass::Part part[kWarps], part_out;
 };
 
@@ -55,13 +56,14 @@ __global__ void __launch_bounds__(kThreads, 2) lazy_greedy_kernel(LazyGreedyPara
                                               : SPEC_REQ_OK;
         if (lane == 0) sm.st = st;
     }
+    if (tid == 0) sm.dbgv = 0;
     __syncthreads();
 
     int st = sm.st, node = 0, L = 0, a = -1;
     while (st == SPEC_REQ_OK) {
         const char *row = reinterpret_cast<const char *>(P.logits) + (base + node) * (size_t)P.V * kEsz;
         const rowpass::Part p = rowpass::cta_row_stats<DT, ROW_GREEDY, kThreads, 4>(
-            row, P.V, 0.f, sm.part, &sm.part_out);
+            row, P.V, 0.f, sm.part, &sm.part_out, &sm.dbgv);
         if (p.flags) {
             st = SPEC_REQ_BAD_ROW;
             break;
@@ -77,12 +79,35 @@ __global__ void __launch_bounds__(kThreads, 2) lazy_greedy_kernel(LazyGreedyPara
         __syncthreads();
         const int next = sm.next;
         if (next < 0) break;
+        if (kDebug && !(L < N - 1 && next >= 1 && next < N)) {
+            if (tid == 0) sm.dbgv |= DBG_WALK;
+            break;
+        }
         if (tid == 0) sm.path[L] = next;
         ++L;
         node = next;
         __syncthreads();
     }
     __syncthreads();
+    if constexpr (kDebug) {
+        // the accepted path is a chain of parent links and the bonus a token
+        if (tid == 0) {
+            int v = sm.dbgv;
+            if (st == SPEC_REQ_OK) {
+                int prev = 0;
+                for (int j = 0; j < L; ++j) {
+                    const int nd = sm.path[j];
+                    if (nd < 1 || nd >= N || sm.par[nd] != prev) v |= DBG_WALK;
+                    prev = nd >= 0 && nd < N ? nd : 0;
+                }
+                if (!(a >= 0 && a < P.V)) v |= DBG_WALK;
+            }
+            if (v && P.dbg) atomicOr(P.dbg + b, v);
+            sm.dbgv = v;
+        }
+        __syncthreads();
+        if (sm.dbgv) st = SPEC_REQ_INTERNAL;
+    }
     for (int j = tid; j < N; j += kThreads) {
         int ot = -1, kv = -1;
         if (st == SPEC_REQ_OK) {

@@ -15,9 +15,15 @@
 
 using namespace specv;
 
-// argmax of SPEC_NOALLOC_MAX_ROWS rows, then their flags: 2 * 16384 * 4 bytes = 128 KiB.
-// Every GPU that loads this library holds the array until the process exits.
-static __device__ __align__(256) int32_t g_noalloc_scratch[2 * SPEC_NOALLOC_MAX_ROWS];
+// argmax of SPEC_NOALLOC_MAX_ROWS rows, then their flags: 2 * 16384 * 4 bytes = 128 KiB
+// (the debug build adds one violation word per request, 64 KiB more). Every GPU that loads
+// this library holds the array until the process exits.
+#ifdef SPEC_DEBUG
+constexpr int kScratchWords = 3 * SPEC_NOALLOC_MAX_ROWS;
+#else
+constexpr int kScratchWords = 2 * SPEC_NOALLOC_MAX_ROWS;
+#endif
+static __device__ __align__(256) int32_t g_noalloc_scratch[kScratchWords];
 
 namespace {
 
@@ -142,6 +148,15 @@ extern "C" int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, 
 
     // Every row's argmax and flags are written by the first kernel before the walk reads
     // them, so nothing left in the array by an earlier call needs clearing.
+    int32_t *dbg = nullptr;
+#ifdef SPEC_DEBUG
+    // debug builds: the requests' violation words, zeroed for this call
+    dbg = scratch + 2 * SPEC_NOALLOC_MAX_ROWS;
+    if (cudaMemsetAsync(dbg, 0, sizeof(int32_t) * (size_t)B, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+    }
+#endif
     RowStatsParams rp{};
     rp.x = logits;
     rp.V = V;
@@ -152,6 +167,7 @@ extern "C" int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, 
     rp.s = nullptr;
     rp.arg = arg;
     rp.flags = flags;
+    rp.dbg = dbg;
     if (launch_row_stats(rp, dtype, ROW_GREEDY, st) != cudaSuccess) return SPEC_ERR_CUDA;
 
     GreedyWalkParams gp;
@@ -167,6 +183,7 @@ extern "C" int spec_verify_greedy_noalloc(const void *logits, int dtype, int B, 
     gp.out.kv_commit = kv_commit;
     gp.out.bonus = bonus;
     gp.out.status = status;
+    gp.dbg = dbg;
     if (launch_walk_greedy(gp, st) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }

@@ -166,6 +166,25 @@ struct Part {
     int arg, flags;
 };
 
+// Vector idx of a row of n 16-byte vectors. Debug builds check the index first and, when it
+// is outside the row, record the violation and return zeros instead of loading.
+__device__ __forceinline__ uint4 ldg_checked(const uint4 *row, int idx, int n, int32_t *dbg,
+                                             int b) {
+    if (!dbg_check(idx >= 0 && idx < n, dbg, b, DBG_INDEX)) return make_uint4(0, 0, 0, 0);
+    return ldg_stream(row + idx);
+}
+
+// The same, recording a violation in a shared-memory word of the CTA (when given).
+__device__ __forceinline__ uint4 ldg_flagged(const uint4 *row, int idx, int n, int *flag) {
+    if constexpr (kDebug) {
+        if (!(idx >= 0 && idx < n)) {
+            if (flag) atomicOr(flag, DBG_INDEX);
+            return make_uint4(0, 0, 0, 0);
+        }
+    }
+    return ldg_stream(row + idx);
+}
+
 template <int MODE>
 __device__ __forceinline__ Part merge(Part x, Part y, float k) {
     Part r;
@@ -198,10 +217,12 @@ __device__ __forceinline__ Part warp_merge(Part p, float k) {
 
 // One CTA streams one row: returns the merged statistics to every thread. THREADS must match
 // blockDim.x; sh_part needs THREADS / 32 entries. Same per-element arithmetic as the
-// one-CTA-per-row kernel.
+// one-CTA-per-row kernel. Debug builds check every vector index and set DBG_INDEX in the
+// shared word *flag (when given) instead of loading outside the row.
 template <int DT, int MODE, int THREADS, int UNROLL>
 __device__ __forceinline__ Part cta_row_stats(const char *rowp, int64_t V, float k,
-                                              Part *sh_part, Part *sh_out) {
+                                              Part *sh_part, Part *sh_out,
+                                              int *flag = nullptr) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;
     constexpr int kW = THREADS / 32;
@@ -219,7 +240,7 @@ __device__ __forceinline__ Part cta_row_stats(const char *rowp, int64_t V, float
     for (; i + (UNROLL - 1) * THREADS < nv; i += UNROLL * THREADS) {
         uint4 w[UNROLL];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) w[u] = ldg_stream(vb + i + u * THREADS);
+        for (int u = 0; u < UNROLL; ++u) w[u] = ldg_flagged(vb, i + u * THREADS, nv, flag);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int e0 = (int)head + (i + u * THREADS) * kEpv;
@@ -230,7 +251,7 @@ __device__ __forceinline__ Part cta_row_stats(const char *rowp, int64_t V, float
         }
     }
     for (; i < nv; i += THREADS) {
-        const uint4 w = ldg_stream(vb + i);
+        const uint4 w = ldg_flagged(vb, i, nv, flag);
         const int e0 = (int)head + i * kEpv;
         if (DT == 1)
             proc_bf16<MODE>(a, w, e0, k);

@@ -30,19 +30,12 @@ namespace {
 
 using namespace rowpass;
 
-#ifndef SPEC_ROW_UNROLL
-#define SPEC_ROW_UNROLL 4   // 16-byte loads in flight per thread
-#endif
-#ifndef SPEC_ROW_MIN_CTAS
-#define SPEC_ROW_MIN_CTAS 6   // resident CTAs per SM the register budget is sized for
-#endif
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = SPEC_ROW_UNROLL;
 // The statistics of one row: row blockIdx.x (blockIdx.x - first for the second set of a
 // paired launch), or, with SPLIT > 1, piece blockIdx.x % SPLIT of row blockIdx.x / SPLIT.
-template <int DT, int MODE, bool SECOND, int SPLIT = 1>
+template <int DT, int MODE, bool SECOND, int SPLIT = 1, int kUnroll = SPEC_ROW_UNROLL>
 __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;   // elements per 16-byte vector
@@ -53,6 +46,10 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
     const int cta = SECOND ? (int)blockIdx.x - first : (int)blockIdx.x;
     const int row = cta / SPLIT, piece = cta - row * SPLIT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // debug builds: the request a violation is charged to (clamped into the batch)
+    int32_t *const dbg = P.dbg;
+    const int dbg_b = min(row, P.rows - 1) / P.N;
+    if (!dbg_check(row < P.rows, dbg, dbg_b, DBG_INDEX)) return;
     const int64_t V = P.V;
     const char *rowp = reinterpret_cast<const char *>(P.x) + (size_t)row * (size_t)V * kEsz;
 
@@ -75,7 +72,7 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
             if (c >= 1 && c < nb && P.parent[(size_t)b * N + c] == n) {
                 any = true;
                 const int t = P.tok[(size_t)b * N + c];
-                if (t >= 0 && t < V) {
+                if (t >= 0 && t < V && dbg_check(c < N, dbg, dbg_b, DBG_INDEX)) {
                     child[h] = c;
                     if (gather) zc[h] = load_elem<DT>(rowp, t);   // prefetch, used at the end
                 }
@@ -105,14 +102,16 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
     const bool aligned = head == 0;
     const int g = piece * kChunksPerCta + tid / kGroup, gt = tid % kGroup;   // chunk, rank
     const int v1 = row_chunk_vec(g + 1, nv, V, aligned, kEpv);
-    if (g == 0 && gt < head) proc_scalar<MODE>(a, load_elem<DT>(rowp, gt), gt, k);
+    if (g == 0 && gt < head && dbg_check(gt < V, dbg, dbg_b, DBG_INDEX))
+        proc_scalar<MODE>(a, load_elem<DT>(rowp, gt), gt, k);
 
     const uint4 *vb = reinterpret_cast<const uint4 *>(rowp + head * kEsz);
     int i = row_chunk_vec(g, nv, V, aligned, kEpv) + gt;
     for (; i + (kUnroll - 1) * kGroup < v1; i += kUnroll * kGroup) {
         uint4 w[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kGroup);
+        for (int u = 0; u < kUnroll; ++u)
+            w[u] = ldg_checked(vb, i + u * kGroup, nv, dbg, dbg_b);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int e0 = (int)head + (i + u * kGroup) * kEpv;
@@ -123,7 +122,7 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
         }
     }
     for (; i < v1; i += kGroup) {
-        const uint4 w = ldg_stream(vb + i);
+        const uint4 w = ldg_checked(vb, i, nv, dbg, dbg_b);
         const int e0 = (int)head + i * kEpv;
         if (DT == 1)
             proc_bf16<MODE>(a, w, e0, k);
@@ -145,7 +144,9 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
     // warps of one chunk first (consecutive lanes), then across chunks
 #pragma unroll
     for (int o = 1; o < kWarpsPerGroup; o <<= 1) p = merge<MODE>(p, shfl_part(p, o), k);
-    if (MODE == ROW_SAMPLE && P.chunk && aligned && lane < kWarps && lane % kWarpsPerGroup == 0)
+    if (MODE == ROW_SAMPLE && P.chunk && aligned && lane < kWarps && lane % kWarpsPerGroup == 0 &&
+        dbg_check(piece * kChunksPerCta + lane / kWarpsPerGroup < kRowChunks, dbg, dbg_b,
+                  DBG_INDEX))
         P.chunk[(size_t)row * kRowChunks + piece * kChunksPerCta + lane / kWarpsPerGroup] =
             make_float2(p.m, p.s);
 #pragma unroll
@@ -159,7 +160,10 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
         if (lane == 0) {
             parts[piece] = RowPart{p.m, p.s, p.arg, p.flags};
             __threadfence();
-            last = atomicAdd(&P.count[row], 1) == SPLIT - 1;
+            const int old = atomicAdd(&P.count[row], 1);
+            // the counter is zero between launches, so the arrivals see 0 .. SPLIT-1
+            dbg_check(old >= 0 && old < SPLIT, dbg, dbg_b, DBG_ARRIVAL);
+            last = old == SPLIT - 1;
         }
         if (!__shfl_sync(0xffffffffu, last, 0)) return;
         __threadfence();
@@ -200,7 +204,7 @@ __device__ __forceinline__ void row_stats_row(const RowStatsParams P, int first)
 }
 
 template <int DT, int MODE>
-__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(RowStatsParams P) {
+__global__ void __launch_bounds__(kThreads, kRowCtasPerSm) row_stats_kernel(RowStatsParams P) {
     grid_dep_wait();     // the logits (and the tree) come from earlier kernels
     grid_dep_launch();   // the walk may start launching: it waits for this grid's results
     row_stats_row<DT, MODE, false>(P, 0);
@@ -209,14 +213,14 @@ __global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS) row_stats_kernel(
 // Target rows and dense-draft rows in one launch (the first A.rows CTAs take the target rows):
 // both sets are streamed at once instead of one launch after the other.
 template <int DT1, int MODE1, int DT2, int MODE2>
-__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, SPEC_PAIR_MIN_CTAS)
     row_stats_pair_kernel(RowStatsParams A, RowStatsParams B) {
     grid_dep_wait();
     grid_dep_launch();
     if ((int)blockIdx.x < A.rows)
-        row_stats_row<DT1, MODE1, false>(A, 0);
+        row_stats_row<DT1, MODE1, false, 1, SPEC_PAIR_UNROLL>(A, 0);
     else
-        row_stats_row<DT2, MODE2, true>(B, A.rows);
+        row_stats_row<DT2, MODE2, true, 1, SPEC_PAIR_UNROLL>(B, A.rows);
 }
 
 template <int DT1, int DT2, int MODE2>
@@ -236,11 +240,11 @@ cudaError_t launch_pair_d(const RowStatsParams &a, const RowStatsParams &b, int 
 // Small batches: SPLIT CTAs per row (each streaming kRowChunks / SPLIT chunks) so that one
 // wave of CTAs covers the GPU.
 template <int DT, int MODE, int SPLIT>
-__global__ void __launch_bounds__(kThreads, SPEC_ROW_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, kSplitCtasPerSm)
     row_stats_split_kernel(RowStatsParams P) {
     grid_dep_wait();
     grid_dep_launch();
-    row_stats_row<DT, MODE, false, SPLIT>(P, 0);
+    row_stats_row<DT, MODE, false, SPLIT, SPEC_SPLIT_UNROLL>(P, 0);
 }
 
 template <int DT, int MODE>

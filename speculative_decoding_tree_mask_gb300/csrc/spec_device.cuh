@@ -11,6 +11,27 @@ namespace specv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kNone = 0x7fffffff;   // "no index yet" in argmax reductions
 
+// Debug flavour (compiled with SPEC_DEBUG): the kernels check the indices they compute and
+// the split rows' arrival counters. A failed check sets a bit in the request's debug word
+// (a per-request int32 array of the handle) and the offending access is skipped; the walk
+// that finishes the request then reports SPEC_REQ_INTERNAL instead of its result. Nothing
+// traps. In release builds every check is the constant true and compiles to nothing.
+#ifdef SPEC_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+enum { DBG_INDEX = 1, DBG_ARRIVAL = 2, DBG_WALK = 4 };
+
+__device__ __forceinline__ bool dbg_check(bool ok, int32_t *words, int b, int bit) {
+    if constexpr (kDebug) {
+        if (!ok && words) atomicOr(words + b, bit);
+        return ok;
+    } else {
+        return true;
+    }
+}
+
 // Number of nodes request b verifies under a node budget: all N without one, the budget when
 // it lies in [1, N], and 0 (the request is refused) otherwise.
 __device__ __forceinline__ int node_budget(const int32_t *n_active, int b, int N) {

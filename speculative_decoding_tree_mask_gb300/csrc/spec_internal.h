@@ -51,6 +51,33 @@ cudaError_t launch_dependent_cluster(void (*kernel)(Params...), dim3 grid, dim3 
 
 constexpr int kMaxN = 64;   // nodes per request (one 64-bit ancestor mask)
 
+// Shapes of the row-statistics stream. The one-CTA-per-row kernel keeps SPEC_ROW_MIN_CTAS
+// CTAs of 256 threads on every SM with SPEC_ROW_UNROLL 16-byte loads in flight per thread;
+// the split kernel (small batches: several CTAs per row, one wave) has its own pair, since
+// with fewer CTAs than the GPU can hold it can trade occupancy for bytes in flight.
+#ifndef SPEC_ROW_UNROLL
+#define SPEC_ROW_UNROLL 4
+#endif
+#ifndef SPEC_ROW_MIN_CTAS
+#define SPEC_ROW_MIN_CTAS 6
+#endif
+#ifndef SPEC_SPLIT_UNROLL
+#define SPEC_SPLIT_UNROLL 4
+#endif
+#ifndef SPEC_SPLIT_MIN_CTAS
+#define SPEC_SPLIT_MIN_CTAS 6
+#endif
+// The paired target + dense-draft launch likewise: its dense-draft rows keep more values live,
+// which at 6 CTAs per SM (40 registers) spilled; 5 per SM fit without spills.
+#ifndef SPEC_PAIR_UNROLL
+#define SPEC_PAIR_UNROLL 4
+#endif
+#ifndef SPEC_PAIR_MIN_CTAS
+#define SPEC_PAIR_MIN_CTAS 5
+#endif
+constexpr int kRowCtasPerSm = SPEC_ROW_MIN_CTAS;
+constexpr int kSplitCtasPerSm = SPEC_SPLIT_MIN_CTAS;
+
 enum RowMode { ROW_GREEDY = 0, ROW_SAMPLE = 1, ROW_PROBS = 2 };
 
 // Row chunks: the row-statistics stream splits every row into kRowChunks contiguous pieces
@@ -116,6 +143,7 @@ struct RowStatsParams {
     RowPart *piece = nullptr;
     int32_t *count = nullptr;
     int split = 1;
+    int32_t *dbg = nullptr;   // debug builds: per-request violation bits [B] (may be null)
 };
 
 cudaError_t launch_row_stats(const RowStatsParams &p, int dtype, int mode, cudaStream_t st);
@@ -142,6 +170,7 @@ struct GreedyWalkParams {
     const int32_t *arg, *flags;   // row statistics [B, N]
     WalkOutputs out;
     const int32_t *n_active = nullptr;
+    int32_t *dbg = nullptr;       // debug builds: per-request violation bits [B]
 };
 
 cudaError_t launch_walk_greedy(const GreedyWalkParams &p, cudaStream_t st);
@@ -155,6 +184,7 @@ struct LazyGreedyParams {
     const int32_t *parent, *tok;
     WalkOutputs out;
     const int32_t *n_active = nullptr;
+    int32_t *dbg = nullptr;       // debug builds: per-request violation bits [B]
 };
 
 cudaError_t launch_lazy_greedy(const LazyGreedyParams &p, cudaStream_t st);
@@ -182,6 +212,7 @@ struct SampleWalkParams {
     // Eager walks: CTAs per request (1, 2, 4 or 8), one thread-block cluster each; the
     // cluster splits every vocabulary pass of its request.
     int cluster = 1;
+    int32_t *dbg = nullptr;       // debug builds: per-request violation bits [B]
 };
 
 // KV commit of the accepted path into a paged cache (see spec_kv_commit).
@@ -217,8 +248,6 @@ struct BudgetParams {
 
 cudaError_t launch_budget_update(const BudgetParams &p, cudaStream_t st);
 
-// Dynamic shared memory the sampling walk needs for vocabulary size V.
-size_t walk_sample_smem(int64_t V);
 cudaError_t launch_walk_sample(const SampleWalkParams &p, cudaStream_t st);
 
 }  // namespace specv

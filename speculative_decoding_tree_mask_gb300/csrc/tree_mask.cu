@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
         }
     }
     bad = __any_sync(0xffffffffu, bad);
+    bool viol = false;   // debug builds: a hop outside the request's nodes
     if (!bad) {
         __syncwarp();
 #pragma unroll 1
@@ -53,7 +54,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
                 if (i < N) {
                     const int j = s_hop[warp][i];
                     na[h] = s_anc[warp][i];
-                    if (j >= 0) {
+                    if (kDebug && j >= N) {
+                        viol = true;
+                    } else if (j >= 0) {
                         na[h] |= s_anc[warp][j];
                         nh[h] = s_hop[warp][j];
                     }
@@ -80,7 +83,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
             depth_out[(size_t)b * N + i] = bad ? -1 : __popcll(a) - 1;
         }
     }
-    if (lane == 0) status[b] = bad ? 1 : 0;
+    if (kDebug) viol = __any_sync(0xffffffffu, viol);
+    if (lane == 0) status[b] = bad ? 1 : (viol ? SPEC_REQ_INTERNAL : 0);
 }
 
 }  // namespace

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
              : __any_sync(full, bad_par) ? SPEC_REQ_BAD_PARENT
              : __any_sync(full, bad_tok) ? SPEC_REQ_BAD_TOKEN
                                          : SPEC_REQ_OK;
+    bool viol = false;   // debug builds: a check of this walk failed
 
     int L = 0, node = 0, a = -1;
     int pth0 = -1, pth1 = -1;   // path[j] lives in lane j % 32, slot j / 32
@@ -71,6 +72,10 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
                 c = 32 + __ffs(m1) - 1;
             else
                 break;
+            if (!dbg_check(c >= 1 && c < nb && L < N - 1, P.dbg, b, DBG_WALK)) {
+                viol = true;
+                break;
+            }
             if (lane == (L & 31)) {
                 if (L < 32)
                     pth0 = c;
@@ -85,6 +90,28 @@ __global__ void __launch_bounds__(32 * kGreedyWarps) walk_greedy_kernel(GreedyWa
     // Compaction: out_tokens = tokens of path[0..L) then the bonus; kv_commit = 0, path.
     const int prev0 = __shfl_sync(full, pth0, (lane + 31) & 31);
     const int prev1 = __shfl_sync(full, pth1, (lane + 31) & 31);
+    if constexpr (kDebug) {
+        // The accepted path is a chain of parent links from the root, the bonus a token, and
+        // no row statistics of this request failed a check.
+        if (st == 0) {
+            bool bad = !(a >= 0 && a < P.V);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = lane + 32 * h;
+                const int nd = h == 0 ? pth0 : pth1;
+                const int pv = j == 0 ? 0 : (h == 0 ? prev0 : (lane == 0 ? prev0 : prev1));
+                const int pa = __shfl_sync(full, par[0], nd & 31);
+                const int pb = __shfl_sync(full, par[1], nd & 31);
+                if (j < L) bad |= nd < 1 || nd >= nb || (nd < 32 ? pa : pb) != pv;
+            }
+            if (__any_sync(full, bad)) {
+                dbg_check(false, P.dbg, b, DBG_WALK);
+                viol = true;
+            }
+        }
+        if (P.dbg && P.dbg[b] != 0) viol = true;
+        if (viol) st = SPEC_REQ_INTERNAL;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int j = lane + 32 * h;

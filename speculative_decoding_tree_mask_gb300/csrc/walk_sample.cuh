@@ -54,6 +54,20 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSub = kSubTile;   // elements per sub-tile: 32 lanes x 8
 
+// Eager point-draft bonus draws: the pass over the chosen row chunk also keeps the raw 16-byte
+// vectors of its sub-tiles in shared memory (up to kStageBytes), so the final search reads its
+// sub-tile there instead of loading it a second time.
+constexpr int kStageBytes = 48 * 1024;
+template <int DT>
+constexpr int stage_vecs() { return DT == 1 ? 1 : 2; }   // 16-byte vectors per lane per sub-tile
+template <int DT>
+constexpr int stage_subs() { return kStageBytes / (32 * 16 * stage_vecs<DT>()); }
+// Floats of the sub-tile sums in dynamic shared memory (a multiple of 4: the staging area
+// after them starts 16-byte aligned).
+__host__ __device__ __forceinline__ int subsum_floats(int64_t V) {
+    return (int)(((V + kSub - 1) / kSub + 3) & ~int64_t(3));
+}
+
 enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z, CMD_STATS };
 
 struct Smem {
@@ -83,7 +97,19 @@ struct Smem {
     rowpass::Part part[kWarps], part_out;
     double ctot;   // clusters: this CTA's share of a pass total
     int bcast;     // clusters: a control value of the leading CTA
+    int dbgv;      // debug builds: violation bits found by this CTA
 };
+
+// Debug builds: record a violation found while walking request (CTA) state in shared memory;
+// it is charged to the request when the walk ends. Returns `ok` (always true in release).
+__device__ __forceinline__ bool walk_check(bool ok, Smem &sm, int bit) {
+    if constexpr (kDebug) {
+        if (!ok) atomicOr(&sm.dbgv, bit);
+        return ok;
+    } else {
+        return true;
+    }
+}
 
 // Clusters (CL CTAs per request): every CTA runs the same walk on the same data, but each
 // branch that is followed by a cluster barrier takes the leading CTA's value, so all CTAs
@@ -246,7 +272,7 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
 // order).
 template <int DT, int DK, int DDT, int CL = 1>
 __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0,
-                              int jhi = INT_MAX, bool total = true) {
+                              int jhi = INT_MAX, bool total = true, uint4 *stage = nullptr) {
     // sub-tiles in flight per warp (32 registers of raw loads)
     constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : SPEC_DENSE_PASS_UNROLL;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
@@ -276,13 +302,18 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
             const int j = j0 + u * GW;
             if (j < nfull) {
                 float zs[8], ds[8], r[8];
+                if (DK == DRAFT_POINT && stage) {   // the caller staged only full sub-tiles
+                    uint4 *sp = stage + ((size_t)(j - jlo) * 32 + lane) * stage_vecs<DT>();
+                    sp[0] = za[u];
+                    if (DT == 0) sp[1] = zb[u];
+                }
                 shifted8<DT>(za[u], zb[u], c.negm, zs);
                 if (DK == DRAFT_LOGITS && c.useq) shifted8<kDDT>(da[u], db[u], c.negmq, ds);
                 if (DK == DRAFT_PROBS_F32 && c.useq) shifted8<0>(da[u], db[u], 0.f, ds);
                 residual8<DK>(c, sm, zs, ds, r);
                 if (DK == DRAFT_POINT) zero_rejected(sm, j, lane, rc, r);
                 const float incl = warp_incl_scan(sum8(r));
-                if (lane == 31) {
+                if (lane == 31 && walk_check(j < (c.V + kSub - 1) / kSub, sm, DBG_INDEX)) {
                     subsum[j] = incl;
                     wsum.add(incl);
                 }
@@ -300,7 +331,7 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
         float r[8];
         residual8_any<DT, DK, DDT>(c, sm, j, lane, rc, r);
         const float incl = warp_incl_scan(sum8(r));
-        if (lane == 31) {
+        if (lane == 31 && walk_check(j < (c.V + kSub - 1) / kSub, sm, DBG_INDEX)) {
             subsum[j] = incl;
             wsum.add(incl);
         }
@@ -367,64 +398,70 @@ __device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum, 
 }
 
 // Inverse CDF over the stored sub-tile sums of [jlo, jhi) (warp 0; default: the whole row):
-// the bonus token for tau = u * (sum of the range), or for the given tau_abs >= 0; -1 when the
-// residual sums to zero there.
+// the bonus token for tau = u * (sum of the range), or for the given tau_abs >= 0 (relative to
+// the start of the range); -1 when the residual sums to zero there. One loop narrows the range
+// 32 candidates at a time -- groups of consecutive sub-tiles (each lane's group summed with
+// compensation), then single sub-tiles -- and a last step searches the 32 lanes x 8 elements
+// of the chosen sub-tile. All of it is float arithmetic: every term is a non-negative mass, so
+// a prefix formed by a compensated lane sum and a 32-wide scan is within about 7 float
+// roundings (4e-7 relative) of its value, inside the 1e-6 * S margin draws are compared on.
+// The walk's warp executes this code once per draw, and instruction fetch dominates such cold
+// code on this part (the no-instruction stall): one loop body serving every level keeps it
+// short. When rounding leaves tau at or past the end of the range, each level takes its last
+// candidate with mass, so the draw is the range's last token with r > 0.
 template <int DT, int DK, int DDT>
 __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, float u,
-                            int jlo = 0, int jhi = -1, double tau_abs = -1.0) {
+                            int jlo = 0, int jhi = -1, double tau_abs = -1.0,
+                            const uint4 *stage = nullptr) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     if (jhi < 0) jhi = (c.V + kSub - 1) / kSub;
-    const int nsub = jhi - jlo;
-    // level 1: every lane sums a contiguous chunk of sub-tiles; scan the chunk totals
-    const int cs = (nsub + 31) / 32;
-    const int lo = jlo + min(lane * cs, nsub), hi = jlo + min(lane * cs + cs, nsub);
-    KSum chunk;
-    for (int j = lo; j < hi; ++j) chunk.add(subsum[j]);
-    const double incl = warp_incl_scan_d(chunk.value());
-    const double S = __shfl_sync(full, incl, 31);
-    if (!(S > 0.0)) return -1;
-    double excl = __shfl_up_sync(full, incl, 1);
-    if (lane == 0) excl = 0.0;
-    const double tau = tau_abs >= 0.0 ? tau_abs : (double)u * S;
-    const unsigned ball = __ballot_sync(full, incl > tau);
-    if (ball == 0) return last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
-    const int owner = __ffs(ball) - 1;
-    const int olo = __shfl_sync(full, lo, owner), ohi = __shfl_sync(full, hi, owner);
-    double base = __shfl_sync(full, excl, owner);
-    // level 2: the owner's chunk, 32 sub-tiles at a time, one lane per sub-tile
-    int js = -1, jlast = -1;
-    double pref = 0.0, plast = 0.0;
-    for (int g = olo; g < ohi && js < 0; g += 32) {
-        const int j = g + lane;
-        const float sj = j < ohi ? subsum[j] : 0.f;
-        const double in2 = warp_incl_scan_d((double)sj);
-        double ex2v = __shfl_up_sync(full, in2, 1);
-        if (lane == 0) ex2v = 0.0;
-        const unsigned hit = __ballot_sync(full, j < ohi && base + in2 > tau);
-        const unsigned pos = __ballot_sync(full, j < ohi && sj > 0.f);
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            js = g + l;
-            pref = base + __shfl_sync(full, ex2v, l);
-        } else if (pos) {
-            const int l = 31 - __clz(pos);
-            jlast = g + l;
-            plast = base + __shfl_sync(full, ex2v, l);
+    int j0 = jlo, n = jhi - jlo;
+    float tau = (float)tau_abs;   // negative: u * (the range's total), set below
+    for (bool top = true; top || n > 1; top = false) {
+        const int w = (n + 31) / 32;   // sub-tiles per candidate
+        const int a = j0 + min(lane * w, n), z = j0 + min(lane * w + w, n);
+        KSum g;
+        for (int j = a; j < z; ++j) g.add(subsum[j]);
+        const float m = g.s - g.c;
+        const float incl = warp_incl_scan(m);
+        if (top) {
+            const float tot = __shfl_sync(full, incl, 31);
+            if (!(tot > 0.f)) return -1;
+            if (tau < 0.f) tau = u * tot;
         }
-        base += __shfl_sync(full, in2, 31);
+        float excl = __shfl_up_sync(full, incl, 1);
+        if (lane == 0) excl = 0.f;
+        const unsigned hit = __ballot_sync(full, incl > tau);
+        int l;
+        if (hit) {
+            l = __ffs(hit) - 1;
+        } else {   // rounding: tau at or past the end; follow the last candidate with mass
+            const unsigned pos = __ballot_sync(full, m > 0.f);
+            if (!pos) return last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
+            l = 31 - __clz(pos);
+            tau = INFINITY;
+        }
+        tau -= __shfl_sync(full, excl, l);
+        j0 = __shfl_sync(full, a, l);
+        n = __shfl_sync(full, z, l) - j0;
     }
-    if (js < 0) {   // rounding between the two levels: take the chunk's last positive sub-tile
-        js = jlast;
-        pref = plast;
-    }
-    if (js < 0) return last_positive<DT, DK, DDT>(c, sm, subsum, jlo, jhi);
+    const int js = j0;
 
-    // level 3: re-read sub-tile js; scan its 32 lanes x 8 elements (the pass's arithmetic)
-    const float tr = (float)(tau - pref);
+    // the chosen sub-tile: its 32 lanes x 8 elements (the pass's arithmetic), from the staged
+    // copy when there is one
+    const float tr = tau;
     float r[8];
     int rc = 0;
-    residual8_any<DT, DK, DDT>(c, sm, js, lane, rc, r);
+    if (DK == DRAFT_POINT && stage) {   // the pass staged the range's sub-tiles
+        const uint4 *sp = stage + ((size_t)(js - jlo) * 32 + lane) * stage_vecs<DT>();
+        float zs[8], ds[8];
+        shifted8<DT>(sp[0], DT == 0 ? sp[1] : sp[0], c.negm, zs);
+        residual8<DK>(c, sm, zs, ds, r);
+        zero_rejected(sm, js, lane, rc, r);
+    } else {
+        residual8_any<DT, DK, DDT>(c, sm, js, lane, rc, r);
+    }
     const float inc = warp_incl_scan(sum8(r));
     float exf = __shfl_up_sync(full, inc, 1);
     if (lane == 0) exf = 0.f;
@@ -478,21 +515,24 @@ __device__ void chunk_pick(const Ctx &c, Smem &sm, const float2 *part, int nc, f
         }
         M = mq > 0.0 ? mq : 0.0;
     }
-    const double incl = warp_incl_scan_d(M);
-    const double S = __shfl_sync(full, incl, 31);
+    // float from here on: at most 8 non-negative terms, each within one rounding of its
+    // float64 value, so the scan's prefixes are within a few float roundings of S
+    const float Mf = (float)M;
+    const float incl = warp_incl_scan(Mf);
+    const float S = __shfl_sync(full, incl, 31);
     float Ptot = (float)P;   // only compared with S / 2
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ptot += __shfl_xor_sync(full, Ptot, o);
-    double excl = __shfl_up_sync(full, incl, 1);
-    if (lane == 0) excl = 0.0;
+    float excl = __shfl_up_sync(full, incl, 1);
+    if (lane == 0) excl = 0.f;
     int pick = -1;
-    double tau = 0.0;
-    if (S > 0.0 && S >= 0.5 * (double)Ptot) {
-        tau = (double)u * S;
+    float tau = 0.f;
+    if (S > 0.f && S >= 0.5f * Ptot) {
+        tau = u * S;
         const unsigned hit = __ballot_sync(full, lane < nc && incl > tau);
-        const unsigned pos = __ballot_sync(full, lane < nc && M > 0.0);
+        const unsigned pos = __ballot_sync(full, lane < nc && Mf > 0.f);
         pick = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-        if (pick >= 0) tau = fmax(tau - __shfl_sync(full, excl, pick), 0.0);
+        if (pick >= 0) tau = fmaxf(tau - __shfl_sync(full, excl, pick), 0.f);
     }
     if (lane == 0) {
         sm.cpick = pick;
@@ -622,6 +662,10 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
                 accept = uc * denom < (double)sm.ec[c];   // u < e_t / denom
             }
             if (!accept) {
+                if (!dup && !walk_check(nR < kMaxN, sm, DBG_WALK)) {
+                    w.st = SPEC_REQ_INTERNAL;
+                    continue;
+                }
                 if (!dup) {
                     const int pos = __popc(__ballot_sync(full, r0 < t)) +
                                     __popc(__ballot_sync(full, r1 < t));
@@ -665,6 +709,10 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
                 continue;
             }
         }
+        if (!walk_check(w.L < N - 1 && c >= 1 && c < N, sm, DBG_WALK)) {
+            w.st = SPEC_REQ_INTERNAL;
+            continue;
+        }
         __syncwarp();
         if (lane == 0) sm.path[w.L] = c;
         __syncwarp();
@@ -704,7 +752,9 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
     for (; i + (kUnroll - 1) * kGroup < v1; i += kUnroll * kGroup) {
         uint4 w[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) w[u] = ldg_stream(vb + i + u * kGroup);
+        for (int u = 0; u < kUnroll; ++u)
+            w[u] = walk_check(i + u * kGroup < nv, sm, DBG_INDEX) ? ldg_stream(vb + i + u * kGroup)
+                                                                   : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int e0 = (int)head + (i + u * kGroup) * kEpv;
@@ -715,7 +765,8 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
         }
     }
     for (; i < v1; i += kGroup) {
-        const uint4 w = ldg_stream(vb + i);
+        const uint4 w = walk_check(i < nv, sm, DBG_INDEX) ? ldg_stream(vb + i)
+                                                           : make_uint4(0, 0, 0, 0);
         const int e0 = (int)head + i * kEpv;
         if (DT == 1)
             proc_bf16<ROW_SAMPLE>(a, w, e0, k);
@@ -900,6 +951,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         sm.pending = 0;
         sm.bonus = -1;
         sm.cpart_node = -1;
+        sm.dbgv = 0;
     }
     __syncthreads();
 
@@ -1007,13 +1059,18 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
                 if (warp == 0) chunk_pick(c, sm, part, nc, ub);
                 __syncthreads();
                 q = sm.cpick;
+                if (!walk_check(q < nc, sm, DBG_INDEX)) q = -1;
             }
             if (q >= 0) {
                 const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);
+                // stage the chunk when it fits and holds full sub-tiles only
+                uint4 *stage = !LAZY && jhi - jlo <= stage_subs<DT>() && jhi <= c.V / kSub
+                                   ? reinterpret_cast<uint4 *>(subsum + subsum_floats(c.V))
+                                   : nullptr;
+                residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false, stage);
                 if (warp == 0) {
                     const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
-                                                            sm.ctau);
+                                                            sm.ctau, stage);
                     if (lane == 0) sm.bonus = v;
                 }
                 __syncthreads();
@@ -1045,6 +1102,34 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         }
     }
     __syncthreads();
+    if constexpr (kDebug) {
+        // The accepted path is a chain of parent links from the root; the bonus is a token
+        // and, for point drafts, not one of the stop node's rejected tokens; no row statistics
+        // of this request failed a check. Any violation turns the result into
+        // SPEC_REQ_INTERNAL.
+        if (tid == 0) {
+            int v = sm.dbgv;
+            if (sm.st == 0) {
+                int prev = 0;
+                for (int j = 0; j < sm.L; ++j) {
+                    const int nd = sm.path[j];
+                    if (nd < 1 || nd >= N || sm.par[nd] != prev) v |= DBG_WALK;
+                    prev = nd >= 0 && nd < N ? nd : 0;
+                }
+                if (!(sm.bonus >= 0 && sm.bonus < P.V)) v |= DBG_WALK;
+                if (DK == DRAFT_POINT)
+                    for (int i = 0; i < sm.nR; ++i)
+                        if (sm.R[i] == sm.bonus) v |= DBG_WALK;
+            }
+            if (sm.st == SPEC_REQ_INTERNAL) v |= DBG_WALK;
+            if (P.dbg) {
+                if (v) atomicOr(P.dbg + b, v);
+                if (P.dbg[b]) v |= P.dbg[b];
+            }
+            if (v) sm.st = SPEC_REQ_INTERNAL;
+        }
+        __syncthreads();
+    }
     if (CL > 1 && cluster_rank() != 0) return;   // the leading CTA writes the outputs
 
     // Compaction.
@@ -1075,7 +1160,15 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
-    const size_t smem = sizeof(float) * (size_t)((p.V + kSub - 1) / kSub);   // sub-tile sums
+    // sub-tile sums, then (eager point drafts) the staging area of the bonus chunk
+    const size_t stage = DK == DRAFT_POINT && !p.lazy ? (size_t)kStageBytes : 0;
+    const size_t smem = sizeof(float) * (size_t)subsum_floats(p.V) + stage;
+    if (stage) {
+        const cudaError_t e = cudaFuncSetAttribute(walk_sample_kernel<DT, DK, DDT, false>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     if (!p.lazy) {
         const dim3 block(kThreads);
         // Point drafts pass over one chunk of the stop row at most: a cluster's barriers would

@@ -5,8 +5,6 @@ namespace specv {
 
 cudaError_t launch_walk_sample_dense(const SampleWalkParams &p, cudaStream_t st);
 
-size_t walk_sample_smem(int64_t V) { return sizeof(float) * (size_t)((V + kSub - 1) / kSub); }
-
 cudaError_t launch_walk_sample(const SampleWalkParams &p, cudaStream_t st) {
     if (p.B <= 0) return cudaSuccess;
     if (p.draft_kind != DRAFT_POINT) return launch_walk_sample_dense(p, st);

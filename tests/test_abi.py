@@ -86,3 +86,23 @@ def test_nvtx_ranges_compile(tmp_path):
     for name in _declared() - {"spec_error_string", "spec_profile_begin", "spec_profile_end",
                                "spec_verify_greedy_noalloc"}:
         assert f'SPEC_RANGE("{name}")' in src, name
+
+
+def test_release_build_refuses_the_debug_hooks(lib):
+    """The debug entry points exist in every build; the release build says it is not the
+    debug flavour and refuses the fault-injection and debug-word calls without touching a
+    GPU."""
+    assert lib.spec_debug_build() == 0
+    assert lib.spec_debug_inject_arrival(None, 0, 1) == G.SPEC_ERR_UNSUPPORTED
+    assert lib.spec_debug_words(None, None, 0, None) == G.SPEC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("src", ["api.cu", "row_stats.cu", "walk_greedy.cu", "kv_commit.cu"])
+def test_debug_flavour_compiles(tmp_path, src):
+    """The checked flavour (SPEC_DEBUG) of the entry points and kernels compiles for sm_103a."""
+    import subprocess
+    obj = tmp_path / (src + ".o")
+    r = subprocess.run([B.nvcc(), *B.ARCH, *B.FLAGS, "-DSPEC_DEBUG", "-I", B.INCLUDE, "-I",
+                        B.CSRC, "-c", os.path.join(B.CSRC, src), "-o", str(obj)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
