@@ -8,18 +8,24 @@
 // position seq_pos[b] + j:
 //   block = block_table[b][p / block_size], offset = p % block_size,
 //   NHD cache [num_blocks, block_size, H, D], HND cache [num_blocks, H, block_size, D].
-// fp8 caches hold cvt.rn.satfinite(x / scale) (x / scale rounded to float32 first); the scale
-// is one value per tensor or one per source token (b, node).
-// Work is split into units of (slot j, request b, piece of the slot's H*D elements), ordered
-// slot-major, so that the slots every request commits (j <= accept_len) come first. A grid of
-// 8 CTAs per SM strides over the units: each CTA first reads every request's accepted length
-// and position into shared memory (all loads issued before any is used) and stops at the
-// deepest accepted slot of the batch, so no CTA works on a slot nobody commits. Per unit the
-// node and the cache block are loaded together, the next unit's while this unit's data is in
-// flight, and each thread loads all of its K and V elements of the unit (four 16-byte vectors
-// of each for 16-bit sources) before it stores any of them. The statuses are checked by the
+// fp8 caches hold the fp8 rounding (nearest, ties to even, saturated, the sign kept also when
+// the magnitude rounds to zero) of x / scale rounded to float32 first; the scale is one value
+// per tensor or one per source token (b, node).
+//
+// Work is split into units of (slot j, request b, piece of 4096 of the slot's H*D elements),
+// ordered slot-major, so that the slots every request commits (j <= accept_len) come first.
+// A grid of up to 12 CTAs per SM strides over the units. Each CTA first reads every request's
+// accepted length and position into shared memory and stops at the deepest accepted slot of
+// the batch, so no CTA works on a slot nobody commits; the node of its first unit is loaded in
+// the same round trip. The copy is staged through shared memory with cp.async: each thread
+// copies its own 16-byte vectors of the unit's K and V rows there, waits for its own copies
+// (cp.async.wait_group: a hardware wait on the thread's own group, no spinning) and stores
+// them to the cache, so the data occupies no registers and twelve CTAs fit on an SM. A unit
+// costs two round trips: its node (loaded with the previous unit's data) starts the copies,
+// and its cache block is loaded while they are in flight. The statuses are checked by the
 // CTAs that get the fewest units.
 
+#include <cfloat>
 #include <cuda_fp16.h>
 
 #include "spec_device.cuh"
@@ -29,7 +35,13 @@ namespace specv {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kCtasPerSm = 6;   // resident CTAs per SM the register budget allows
+constexpr int kVecs = 4;                          // 8-element vectors per thread per unit
+constexpr int kUnitElems = kThreads * 8 * kVecs;  // elements of K (and of V) per unit
+constexpr int kCtasPerSm = 12;                    // 16-bit sources: 16 KiB of staging per CTA
+constexpr int kSmemRequests = 1024;               // requests whose (L, position) fit in smem
+
+template <int SRC>
+constexpr int src_bytes() { return SRC == 0 ? 4 : 2; }
 
 template <int SRC>
 __device__ __forceinline__ float src_elem(const void *p, size_t i) {
@@ -39,6 +51,8 @@ __device__ __forceinline__ float src_elem(const void *p, size_t i) {
     return __half2float(__ushort_as_half(h));
 }
 
+// Two fp8 codes: code(a) in the low byte, code(b) in the high byte (nearest, ties to even,
+// saturated at the largest finite value).
 __device__ __forceinline__ uint16_t fp8x2(float a, float b, int kind) {
     uint16_t r;
     if (kind == 1)
@@ -48,10 +62,64 @@ __device__ __forceinline__ uint16_t fp8x2(float a, float b, int kind) {
     return r;
 }
 
-// One scalar element src[si] -> cache[di].
+// fp8 code of a float (nearest, ties to even, saturated; sign-magnitude, so a negative value
+// that rounds to zero is -0: the conversion instruction returns +0 there, so the magnitude is
+// converted and the sign set apart); NaN gives 0x7F.
+template <int CACHE>
+__device__ __forceinline__ uint32_t fp8_of(float q) {
+    if (q != q) return 0x7fu;
+    return (fp8x2(fabsf(q), 0.f, CACHE) & 0xffu) | ((__float_as_uint(q) >> 24) & 0x80u);
+}
+
+// The float32 quotient RN(x / s) for the fp8 encoding, given y = RN(1 / s) for a scale s whose
+// reciprocal is a normal float, without a division. q0 = RN(x y) is within about one ulp of
+// x / s, and one correction with the residual (two fused multiply-adds) leaves q1 within about
+// half an ulp, so RN(x / s) lies within two representable steps of q1. The fp8 code of a value
+// changes only where the value crosses a rounding boundary, a midpoint between two adjacent fp8
+// values. fp8 values are the multiples of 2^(E - KB) in binade E >= Emin (KB mantissa bits) and
+// the multiples of 2^(Emin - KB) below 2^Emin (the subnormals), so in q1's binade e the
+// midpoints are the values whose low 23 - k mantissa bits are exactly 100...0, with
+// k = KB - max(Emin - e, 0) bits kept. When q1's low bits lie more than two steps from that
+// pattern, q1 and RN(x / s) encode alike and q1 is returned with `ok` set; so it is when the
+// residual x - q1 s is exactly zero (q1 is then the exact quotient: a power-of-two scale, or a
+// 16-bit source value that sits on a midpoint itself). Magnitudes beyond
+// Emax saturate to the largest finite value, and those below a quarter of the smallest
+// subnormal round to zero, either way. Anything else (two steps from a midpoint, the binades
+// just under the smallest subnormal, a non-finite value) clears `ok`, and the caller takes the
+// correctly rounded division. The sign is that of x times s (the correction step can turn -0
+// into +0).
+template <int CACHE>
+__device__ __forceinline__ float fp8_quotient(float x, float s, float y, bool &ok) {
+    constexpr int KB = CACHE == 1 ? 3 : 2;           // mantissa bits kept by fp8 normals
+    constexpr int EMIN = CACHE == 1 ? -6 : -14;      // fp8 normal binades [EMIN, EMAX]
+    constexpr int EMAX = CACHE == 1 ? 8 : 15;
+    const float q0 = x * y;
+    const float q1 = fmaf(fmaf(-q0, s, x), y, q0);
+    const uint32_t mag = __float_as_uint(q1) & 0x7fffffffu;
+    const int e = (int)(mag >> 23) - 127;
+    const int k = KB - max(EMIN - e, 0);             // >= 0 for e >= EMIN - KB
+    const uint32_t half = 1u << (22 - max(k, 0));
+    const uint32_t low = mag & (2u * half - 1u);
+    ok = mag < 0x7f800000u &&
+         (e > EMAX || e < EMIN - KB - 2 || (k >= 0 && (low + 2u < half || low > half + 2u)) ||
+          fmaf(-q1, s, x) == 0.f);
+    const uint32_t sign = (__float_as_uint(x) ^ __float_as_uint(s)) & 0x80000000u;
+    return __uint_as_float(mag | sign);
+}
+
+// The correctly rounded division, kept out of line: it runs for a few elements in a million.
+__device__ __noinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
+
+// Whether a scale allows the reciprocal route (its reciprocal is a normal float).
+__device__ __forceinline__ bool recip_ok(float s) {
+    const float a = fabsf(s);
+    return a >= 1e-37f && a <= 1e37f;
+}
+
+// One element src[si] -> cache[di] (the unvectorised path).
 template <int SRC, int CACHE>
 __device__ __forceinline__ void put1(const void *src, size_t si, void *dst, size_t di,
-                                     float scale) {
+                                     float scale, float rcp, bool fast) {
     if (CACHE == 0) {
         if (SRC == 0)
             reinterpret_cast<float *>(dst)[di] = __ldg(reinterpret_cast<const float *>(src) + si);
@@ -59,49 +127,49 @@ __device__ __forceinline__ void put1(const void *src, size_t si, void *dst, size
             reinterpret_cast<unsigned short *>(dst)[di] =
                 __ldg(reinterpret_cast<const unsigned short *>(src) + si);
     } else {
-        const float q = __fdiv_rn(src_elem<SRC>(src, si), scale);
-        reinterpret_cast<uint8_t *>(dst)[di] = (uint8_t)(fp8x2(q, 0.f, CACHE) & 0xff);
+        const float x = src_elem<SRC>(src, si);
+        bool ok = false;
+        float q = fast ? fp8_quotient<CACHE>(x, scale, rcp, ok) : 0.f;
+        if (!ok) q = div_rn(x, scale);
+        reinterpret_cast<uint8_t *>(dst)[di] = (uint8_t)fp8_of<CACHE>(q);
     }
 }
 
-// Raw source elements of one 8-element vector: one 16-byte load (bf16 / f16) or two (f32).
-template <int SRC>
-struct Raw8 {
-    uint4 a, b;
-};
-
-template <int SRC>
-__device__ __forceinline__ Raw8<SRC> load8(const void *src, size_t si) {
-    constexpr int kSrcBytes = SRC == 0 ? 4 : 2;
-    const uint4 *sp =
-        reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(src) + si * kSrcBytes);
-    Raw8<SRC> r;
-    r.a = ldg_stream(sp);
-    if (SRC == 0) r.b = ldg_stream(sp + 1);
-    return r;
+// 16-byte asynchronous copy global -> shared (bypassing L1), and the waits on this thread's
+// copies.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Store one loaded vector at cache element di (16-byte aligned source and destination).
+// Store one staged 8-element vector (`raw`: one 16-byte word for 16-bit sources, two for f32)
+// at cache element di.
 template <int SRC, int CACHE>
-__device__ __forceinline__ void store8(const Raw8<SRC> &r, void *dst, size_t di, float scale) {
+__device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, float scale,
+                                       float rcp, bool fast) {
     if (CACHE == 0) {
-        if (SRC == 0) {
-            uint4 *dp = reinterpret_cast<uint4 *>(reinterpret_cast<char *>(dst) + di * 4);
-            dp[0] = r.a;
-            dp[1] = r.b;
-        } else {
-            *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(dst) + di * 2) = r.a;
-        }
+        uint4 *dp = reinterpret_cast<uint4 *>(reinterpret_cast<char *>(dst) +
+                                              di * (size_t)src_bytes<SRC>());
+        dp[0] = raw[0];
+        if (SRC == 0) dp[1] = raw[1];
         return;
     }
     float x[8];
     if (SRC == 0) {
-        x[0] = __uint_as_float(r.a.x); x[1] = __uint_as_float(r.a.y);
-        x[2] = __uint_as_float(r.a.z); x[3] = __uint_as_float(r.a.w);
-        x[4] = __uint_as_float(r.b.x); x[5] = __uint_as_float(r.b.y);
-        x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
+        const uint4 a = raw[0], b = raw[1];
+        x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+        x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+        x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+        x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
     } else {
-        const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+        const uint4 a = raw[0];
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (SRC == 1) {
@@ -115,28 +183,42 @@ __device__ __forceinline__ void store8(const Raw8<SRC> &r, void *dst, size_t di,
             }
         }
     }
-    uint2 o;
-    uint16_t c[4];
+    float q[8];
+    unsigned slow = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        c[q] = fp8x2(__fdiv_rn(x[2 * q], scale), __fdiv_rn(x[2 * q + 1], scale), CACHE);
-    o.x = uint32_t(c[0]) | (uint32_t(c[1]) << 16);
-    o.y = uint32_t(c[2]) | (uint32_t(c[3]) << 16);
+    for (int i = 0; i < 8; ++i) {
+        bool ok = false;
+        q[i] = fast ? fp8_quotient<CACHE>(x[i], scale, rcp, ok) : 0.f;
+        slow |= ok ? 0u : 1u << i;
+    }
+    if (slow) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (slow & (1u << i)) q[i] = div_rn(x[i], scale);
+    }
+    // the magnitudes in pairs (one conversion per two elements), the signs set apart: the
+    // conversion gives +0 for a negative value that rounds to zero, the format keeps -0
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        c[i] = fp8x2(fabsf(q[2 * i]), fabsf(q[2 * i + 1]), CACHE) |
+               ((__float_as_uint(q[2 * i]) >> 24) & 0x80u) |
+               ((__float_as_uint(q[2 * i + 1]) >> 16) & 0x8000u);
+        if (q[2 * i] != q[2 * i]) c[i] = (c[i] & 0xff00u) | 0x7fu;           // NaN: 0x7F
+        if (q[2 * i + 1] != q[2 * i + 1]) c[i] = (c[i] & 0x00ffu) | 0x7f00u;
+    }
+    uint2 o;
+    o.x = c[0] | (c[1] << 16);
+    o.y = c[2] | (c[3] << 16);
     *reinterpret_cast<uint2 *>(reinterpret_cast<char *>(dst) + di) = o;
 }
 
-// 8-element vectors of K (and as many of V) per thread per unit: 128 bytes of loads in
-// flight per thread for 16-bit sources, 256 for f32.
-template <int SRC>
-constexpr int vecs() { return SRC == 0 ? 2 : 4; }
-constexpr int kUnitElems = kThreads * 8 * 4;      // elements of K (and of V) per unit
-constexpr int kSmemRequests = 4096;               // requests whose (L, position) fit in smem
-
-// Cache element of (slot position `off` in block `blk`, element e of the H*D slot).
+// Cache element of (slot position `off` in block `blk`, element e of the H*D slot). In the
+// NHD layout a slot's H*D elements are contiguous, so no division is needed there.
 __device__ __forceinline__ size_t cache_index(const KvCommitParams &P, int blk, int off, int e) {
+    if (P.layout == 0) return ((size_t)blk * P.block_size + off) * ((size_t)P.H * P.D) + e;
     const int h = e / P.D, d = e - h * P.D;
-    return P.layout == 0 ? (((size_t)blk * P.block_size + off) * P.H + h) * (size_t)P.D + d
-                         : (((size_t)blk * P.H + h) * P.block_size + off) * (size_t)P.D + d;
+    return (((size_t)blk * P.H + h) * P.block_size + off) * (size_t)P.D + d;
 }
 
 // Debug builds: a source or cache index outside its array is skipped and the request's
@@ -162,11 +244,6 @@ __device__ __forceinline__ int last_slot(const KvCommitParams &P, int b) {
     return min(max(P.accept_len[b], 0), P.N - 1);
 }
 
-// One unit of work: slot j of request b, piece `piece` of the slot's H*D elements.
-struct Unit {
-    int j, b, piece, L, pos;
-};
-
 // The request's status: SPEC_REQ_BAD_SLOT if any committed slot maps outside the block table
 // or the cache, else 0. One warp, one lane per slot.
 __device__ __forceinline__ void request_status(const KvCommitParams &P, int b, int L, int pos,
@@ -189,15 +266,46 @@ __device__ __forceinline__ void request_status(const KvCommitParams &P, int b, i
     }
 }
 
+// One unit of work: slot j of request b, piece `piece` of the slot's H*D elements.
+struct Unit {
+    int j, b, piece, L, pos;
+};
+
 template <int SRC, int CACHE, bool VEC>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    kv_commit_kernel(KvCommitParams P, int pieces) {
-    extern __shared__ int s_req[];   // [2][B]: last slot, position of slot 0 (B <= 4096)
+__global__ void __launch_bounds__(kThreads)
+    kv_commit_kernel(KvCommitParams P, int pieces, int cached) {
+    // dynamic shared memory: [staging: K then V rows of one unit][2][B] (last slot, position)
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kRowBytes = kUnitElems * src_bytes<SRC>();
+    uint4 *stage_k = reinterpret_cast<uint4 *>(smem);
+    uint4 *stage_v = reinterpret_cast<uint4 *>(smem + kRowBytes);
+    int *s_req = reinterpret_cast<int *>(smem + (VEC ? 2 * kRowBytes : 0));
     __shared__ int s_max;
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = P.B, N = P.N, G = (int)gridDim.x;
-    const bool cached = B <= kSmemRequests;
+    const int64_t per_slot = (int64_t)B * pieces;
+    // 32-bit division when the unit indices fit (they do for any batch with N*B*pieces < 2^31)
+    const bool small = (int64_t)N * per_slot < (int64_t(1) << 31);
+    auto decode = [&](int64_t u, Unit &x) {
+        if (small) {
+            const uint32_t u32 = (uint32_t)u, ps = (uint32_t)per_slot;
+            x.j = (int)(u32 / ps);
+            const uint32_t r = u32 - (uint32_t)x.j * ps;
+            x.b = (int)(r / (uint32_t)pieces);
+            x.piece = (int)(r - (uint32_t)x.b * (uint32_t)pieces);
+            return;
+        }
+        x.j = (int)(u / per_slot);
+        const int64_t r = u - (int64_t)x.j * per_slot;
+        x.b = (int)(r / pieces);
+        x.piece = (int)(r - (int64_t)x.b * pieces);
+    };
+    // The first unit's node is loaded with the prologue, before its liveness is known (any
+    // unit index names a valid kv_commit entry).
+    Unit first;
+    decode(blockIdx.x, first);
+    const int first_node = __ldg(P.kv_commit + (size_t)first.b * N + first.j);
     int lmax = N - 1;
     if (cached) {
         // Every load of the prologue is issued before any is used: one round trip.
@@ -238,15 +346,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                            cached ? s_req[B + b] : P.seq_pos[b], lane);
 
     const int HD = P.H * P.D;
-    const int64_t per_slot = (int64_t)B * pieces;
     const int64_t units = (int64_t)(max(lmax, 0) + 1) * per_slot;
     // The CTA's next unit at or after u (stride G) that copies something; units when none.
     auto next_live = [&](int64_t u, Unit &x) -> int64_t {
         for (; u < units; u += G) {
-            x.j = (int)(u / per_slot);
-            const int64_t r = u - (int64_t)x.j * per_slot;
-            x.b = (int)(r / pieces);
-            x.piece = (int)(r - (int64_t)x.b * pieces);
+            decode(u, x);
             x.L = cached ? s_req[x.b] : last_slot(P, x.b);
             if (x.j > x.L) continue;   // failed verification, or a slot it does not commit
             x.pos = cached ? s_req[B + x.b] : P.seq_pos[x.b];
@@ -254,74 +358,80 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         return units;
     };
-    // Node and cache block of a unit, loaded together (-1: nothing to copy).
-    auto unit_index = [&](const Unit &x, int &node, int &blk) {
-        const int p = x.pos + x.j;
-        const int bi = p >= 0 ? p / P.block_size : -1;
-        node = __ldg(P.kv_commit + (size_t)x.b * N + x.j);
-        blk = (bi >= 0 && bi < P.max_blocks)
-                  ? __ldg(P.block_table + (size_t)x.b * P.max_blocks + bi)
-                  : -1;
-    };
 
     Unit cur;
     int64_t u = next_live(blockIdx.x, cur);
-    int node = -1, blk = -1;
-    if (u < units) unit_index(cur, node, blk);
+    int node = u == (int64_t)blockIdx.x ? first_node
+                                        : (u < units ? __ldg(P.kv_commit + (size_t)cur.b * N +
+                                                             cur.j)
+                                                     : -1);
     while (u < units) {
-        const int p = cur.pos + cur.j;
-        const bool live = node >= 0 && node < N && blk >= 0 && blk < P.num_blocks && p >= 0;
-        const int off = live ? p - (p / P.block_size) * P.block_size : 0;
         const int b = cur.b;
-        const size_t si = P.scale_per_token ? (size_t)b * N + (live ? node : 0) : 0;
-        const size_t sbase = ((size_t)b * N + (live ? node : 0)) * (size_t)HD;
+        const int p = cur.pos + cur.j;
+        const bool src_ok = node >= 0 && node < N;
+        const size_t sbase = ((size_t)b * N + (src_ok ? node : 0)) * (size_t)HD;
         const int e0 = cur.piece * kUnitElems, e1 = min(HD, e0 + kUnitElems);
-        const int cblk = blk;
-        // The next unit's indices are fetched while this unit's data is in flight.
-        Unit nxt;
-        const int64_t un = next_live(u + G, nxt);
-        if (VEC) {
-            // f32 sources: the unit's 4096 elements in two passes of two vectors each
-            constexpr int kV = vecs<SRC>();
+        if (VEC && src_ok) {
+            // this thread's vectors of the unit's K and V rows -> its own staging slots
 #pragma unroll
-            for (int half = 0; half < 4 / kV; ++half) {
-                Raw8<SRC> k[kV], v[kV];
-#pragma unroll
-                for (int q = 0; q < kV; ++q) {
-                    const int e = e0 + (tid + (half * kV + q) * kThreads) * 8;
-                    if (live && e < e1 &&
-                        kv_index_ok(P, b, sbase + e, cache_index(P, cblk, off, e), 8)) {
-                        k[q] = load8<SRC>(P.src_k, sbase + e);
-                        v[q] = load8<SRC>(P.src_v, sbase + e);
-                    }
-                }
-                if (half == 0 && un < units) unit_index(nxt, node, blk);
-                const float ks = CACHE && live && P.k_scale ? P.k_scale[si] : 1.f;
-                const float vs = CACHE && live && P.v_scale ? P.v_scale[si] : 1.f;
-#pragma unroll
-                for (int q = 0; q < kV; ++q) {
-                    const int e = e0 + (tid + (half * kV + q) * kThreads) * 8;
-                    if (live && e < e1 &&
-                        kv_index_ok(P, b, sbase + e, cache_index(P, cblk, off, e), 8)) {
-                        const size_t di = cache_index(P, cblk, off, e);
-                        store8<SRC, CACHE>(k[q], P.cache_k, di, ks);
-                        store8<SRC, CACHE>(v[q], P.cache_v, di, vs);
+            for (int q = 0; q < kVecs; ++q) {
+                const int e = e0 + (tid + q * kThreads) * 8;
+                if (e < e1) {
+                    const char *sk = reinterpret_cast<const char *>(P.src_k) +
+                                     (sbase + e) * (size_t)src_bytes<SRC>();
+                    const char *sv = reinterpret_cast<const char *>(P.src_v) +
+                                     (sbase + e) * (size_t)src_bytes<SRC>();
+                    const int sl = (tid + q * kThreads) * (SRC == 0 ? 2 : 1);
+                    cp_async16(stage_k + sl, sk);
+                    cp_async16(stage_v + sl, sv);
+                    if (SRC == 0) {
+                        cp_async16(stage_k + sl + 1, sk + 16);
+                        cp_async16(stage_v + sl + 1, sv + 16);
                     }
                 }
             }
+            cp_async_commit();
+        }
+        // the cache block and the scales, while the copies are in flight
+        const int bi = p >= 0 ? p / P.block_size : -1;
+        const int blk = (bi >= 0 && bi < P.max_blocks)
+                            ? __ldg(P.block_table + (size_t)b * P.max_blocks + bi)
+                            : -1;
+        const size_t si = P.scale_per_token ? (size_t)b * N + (src_ok ? node : 0) : 0;
+        const float ks = CACHE && P.k_scale ? P.k_scale[si] : 1.f;
+        const float vs = CACHE && P.v_scale ? P.v_scale[si] : 1.f;
+        // the next unit's node
+        Unit nxt;
+        const int64_t un = next_live(u + G, nxt);
+        const int nnode = un < units ? __ldg(P.kv_commit + (size_t)nxt.b * N + nxt.j) : -1;
+        const bool live = src_ok && blk >= 0 && blk < P.num_blocks;
+        const int off = live ? p - bi * P.block_size : 0;
+        const bool kfast = CACHE && recip_ok(ks), vfast = CACHE && recip_ok(vs);
+        const float krcp = kfast ? __frcp_rn(ks) : 1.f, vrcp = vfast ? __frcp_rn(vs) : 1.f;
+        if (VEC) {
+            if (src_ok) cp_async_wait_all();   // this thread's own copies
+#pragma unroll
+            for (int q = 0; q < kVecs; ++q) {
+                const int e = e0 + (tid + q * kThreads) * 8;
+                if (live && e < e1 &&
+                    kv_index_ok(P, b, sbase + e, cache_index(P, blk, off, e), 8)) {
+                    const size_t di = cache_index(P, blk, off, e);
+                    const int sl = (tid + q * kThreads) * (SRC == 0 ? 2 : 1);
+                    store8<SRC, CACHE>(stage_k + sl, P.cache_k, di, ks, krcp, kfast);
+                    store8<SRC, CACHE>(stage_v + sl, P.cache_v, di, vs, vrcp, vfast);
+                }
+            }
         } else {
-            if (un < units) unit_index(nxt, node, blk);
-            const float ks = CACHE && live && P.k_scale ? P.k_scale[si] : 1.f;
-            const float vs = CACHE && live && P.v_scale ? P.v_scale[si] : 1.f;
             for (int e = e0 + tid; live && e < e1; e += kThreads) {
-                const size_t di = cache_index(P, cblk, off, e);
+                const size_t di = cache_index(P, blk, off, e);
                 if (!kv_index_ok(P, b, sbase + e, di, 1)) continue;
-                put1<SRC, CACHE>(P.src_k, sbase + e, P.cache_k, di, ks);
-                put1<SRC, CACHE>(P.src_v, sbase + e, P.cache_v, di, vs);
+                put1<SRC, CACHE>(P.src_k, sbase + e, P.cache_k, di, ks, krcp, kfast);
+                put1<SRC, CACHE>(P.src_v, sbase + e, P.cache_v, di, vs, vrcp, vfast);
             }
         }
         u = un;
         cur = nxt;
+        node = nnode;
     }
 }
 
@@ -330,13 +440,26 @@ cudaError_t launch_kc(const KvCommitParams &p, bool vec, cudaStream_t st) {
     const int HD = p.H * p.D;
     const int pieces = (HD + kUnitElems - 1) / kUnitElems;
     const int64_t units = (int64_t)p.N * p.B * pieces;
-    const int64_t cap = (int64_t)(p.sms > 0 ? p.sms : 1) * kCtasPerSm;
+    const int cached = p.B <= kSmemRequests;
+    const size_t stage = vec ? 2 * (size_t)kUnitElems * src_bytes<SRC>() : 0;
+    const size_t smem = stage + (cached ? 2 * sizeof(int) * (size_t)p.B : 0);
+    auto kernel = vec ? kv_commit_kernel<SRC, CACHE, true> : kv_commit_kernel<SRC, CACHE, false>;
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    // CTAs resident per SM (12 with 16 KiB of staging; fewer for f32 sources): the grid is one
+    // wave of them at most
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    per_sm = per_sm < kCtasPerSm ? per_sm : kCtasPerSm;
+    const int64_t cap = (int64_t)(p.sms > 0 ? p.sms : 1) * per_sm;
     const int grid = (int)(units < cap ? units : cap);
-    const size_t smem = p.B <= kSmemRequests ? 2 * sizeof(int) * (size_t)p.B : 0;
-    if (vec)
-        kv_commit_kernel<SRC, CACHE, true><<<grid, kThreads, smem, st>>>(p, pieces);
-    else
-        kv_commit_kernel<SRC, CACHE, false><<<grid, kThreads, smem, st>>>(p, pieces);
+    kernel<<<grid, kThreads, smem, st>>>(p, pieces, cached);
     return cudaGetLastError();
 }
 

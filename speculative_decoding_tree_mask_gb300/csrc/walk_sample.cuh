@@ -43,32 +43,56 @@
 namespace specv {
 namespace {
 
+// Sub-tiles in flight per warp in a dense-draft pass: 4 when the target and draft rows are
+// both 16-bit (8 KiB of loads in flight per warp), 2 when either is f32 (4 in flight spilled
+// there).
 #ifndef SPEC_DENSE_PASS_UNROLL
-#define SPEC_DENSE_PASS_UNROLL 2   // sub-tiles in flight per warp in a dense-draft pass
+#define SPEC_DENSE_PASS_UNROLL 4
 #endif
 #ifndef SPEC_LAZY_UNROLL
-#define SPEC_LAZY_UNROLL 6   // 16-byte loads in flight per thread in the lazy row pass
+#define SPEC_LAZY_UNROLL 2   // 16-byte loads in flight per thread in the lazy row pass (rows that are not 16-byte aligned)
+#endif
+// Lazy row passes over 16-byte aligned rows stage their loads through a ring of cp.async
+// copies in shared memory instead: SPEC_LAZY_RING vectors in flight per thread (80 KiB per
+// CTA), twice the register loads, without holding registers.
+#ifndef SPEC_LAZY_RING
+#define SPEC_LAZY_RING 10
 #endif
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSub = kSubTile;   // elements per sub-tile: 32 lanes x 8
 
-// Eager point-draft bonus draws: the pass over the chosen row chunk also keeps the raw 16-byte
-// vectors of its sub-tiles in shared memory (up to kStageBytes), so the final search reads its
-// sub-tile there instead of loading it a second time.
-constexpr int kStageBytes = 48 * 1024;
+// Point-draft bonus draws within one row chunk (chunk_draw): each warp holds up to
+// draw_subs sub-tiles of the chunk in registers.
 template <int DT>
-constexpr int stage_vecs() { return DT == 1 ? 1 : 2; }   // 16-byte vectors per lane per sub-tile
-template <int DT>
-constexpr int stage_subs() { return kStageBytes / (32 * 16 * stage_vecs<DT>()); }
-// Floats of the sub-tile sums in dynamic shared memory (a multiple of 4: the staging area
-// after them starts 16-byte aligned).
+constexpr int draw_subs() { return DT == 1 ? 8 : 4; }
+// Floats of the sub-tile sums in dynamic shared memory.
 __host__ __device__ __forceinline__ int subsum_floats(int64_t V) {
-    return (int)(((V + kSub - 1) / kSub + 3) & ~int64_t(3));
+    return (int)((V + kSub - 1) / kSub);
 }
+// Lazy walks: the cp.async ring follows the sub-tile sums, 16-byte aligned.
+__host__ __device__ __forceinline__ int lazy_ring_offset(int64_t V) {
+    return (subsum_floats(V) + 3) & ~3;
+}
+constexpr size_t kLazyRingBytes = (size_t)kThreads * SPEC_LAZY_RING * 16;
 
 enum { CMD_NONE = 0, CMD_DONE, CMD_BONUS, CMD_PASS_SR, CMD_PASS_Z, CMD_STATS };
+
+// 16-byte asynchronous copy global -> shared (bypassing L1), one commit group per call site,
+// and the wait until at most N of this thread's groups are still in flight (a hardware wait on
+// the thread's own copies: nothing spins).
+__device__ __forceinline__ void cp_async16(uint4 *smem, const uint4 *gmem) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct Smem {
     int par[kMaxN], tok[kMaxN], flags[kMaxN], dflags[kMaxN];
@@ -98,6 +122,8 @@ struct Smem {
     double ctot;   // clusters: this CTA's share of a pass total
     int bcast;     // clusters: a control value of the leading CTA
     int dbgv;      // debug builds: violation bits found by this CTA
+    float dtot[kWarps];      // chunk draw: each warp's block total
+    float dsub[kWarps][8];   // ... and its sub-tile totals
 };
 
 // Debug builds: record a violation found while walking request (CTA) state in shared memory;
@@ -272,9 +298,11 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
 // order).
 template <int DT, int DK, int DDT, int CL = 1>
 __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0,
-                              int jhi = INT_MAX, bool total = true, uint4 *stage = nullptr) {
+                              int jhi = INT_MAX, bool total = true) {
     // sub-tiles in flight per warp (32 registers of raw loads)
-    constexpr int U = DK == DRAFT_POINT ? (DT == 1 ? 8 : 4) : SPEC_DENSE_PASS_UNROLL;
+    constexpr int U = DK == DRAFT_POINT                          ? (DT == 1 ? 8 : 4)
+                      : DT == 1 && DK == DRAFT_LOGITS && DDT == 1 ? SPEC_DENSE_PASS_UNROLL
+                                                                  : 2;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
     constexpr int GW = CL * kWarps;   // warps sharing the pass
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -302,11 +330,6 @@ __device__ void residual_pass(const Ctx &c, Smem &sm, float *subsum, int jlo = 0
             const int j = j0 + u * GW;
             if (j < nfull) {
                 float zs[8], ds[8], r[8];
-                if (DK == DRAFT_POINT && stage) {   // the caller staged only full sub-tiles
-                    uint4 *sp = stage + ((size_t)(j - jlo) * 32 + lane) * stage_vecs<DT>();
-                    sp[0] = za[u];
-                    if (DT == 0) sp[1] = zb[u];
-                }
                 shifted8<DT>(za[u], zb[u], c.negm, zs);
                 if (DK == DRAFT_LOGITS && c.useq) shifted8<kDDT>(da[u], db[u], c.negmq, ds);
                 if (DK == DRAFT_PROBS_F32 && c.useq) shifted8<0>(da[u], db[u], 0.f, ds);
@@ -411,8 +434,7 @@ __device__ int last_positive(const Ctx &c, const Smem &sm, const float *subsum, 
 // candidate with mass, so the draw is the range's last token with r > 0.
 template <int DT, int DK, int DDT>
 __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, float u,
-                            int jlo = 0, int jhi = -1, double tau_abs = -1.0,
-                            const uint4 *stage = nullptr) {
+                            int jlo = 0, int jhi = -1, double tau_abs = -1.0) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     if (jhi < 0) jhi = (c.V + kSub - 1) / kSub;
@@ -448,20 +470,11 @@ __device__ int bonus_search(const Ctx &c, const Smem &sm, const float *subsum, f
     }
     const int js = j0;
 
-    // the chosen sub-tile: its 32 lanes x 8 elements (the pass's arithmetic), from the staged
-    // copy when there is one
+    // the chosen sub-tile: its 32 lanes x 8 elements (the pass's arithmetic), read again
     const float tr = tau;
     float r[8];
     int rc = 0;
-    if (DK == DRAFT_POINT && stage) {   // the pass staged the range's sub-tiles
-        const uint4 *sp = stage + ((size_t)(js - jlo) * 32 + lane) * stage_vecs<DT>();
-        float zs[8], ds[8];
-        shifted8<DT>(sp[0], DT == 0 ? sp[1] : sp[0], c.negm, zs);
-        residual8<DK>(c, sm, zs, ds, r);
-        zero_rejected(sm, js, lane, rc, r);
-    } else {
-        residual8_any<DT, DK, DDT>(c, sm, js, lane, rc, r);
-    }
+    residual8_any<DT, DK, DDT>(c, sm, js, lane, rc, r);
     const float inc = warp_incl_scan(sum8(r));
     float exf = __shfl_up_sync(full, inc, 1);
     if (lane == 0) exf = 0.f;
@@ -568,6 +581,129 @@ __device__ void chunk_marks(const Ctx &c, Smem &sm, const float2 *part, int nc) 
     __syncwarp();
 }
 
+// Point drafts: the bonus token for tau (relative to the start of the chunk's sub-tiles
+// [jlo, jhi)), drawn without a search by one warp. Warp w streams the contiguous sub-tiles
+// [jlo + w per, jlo + (w + 1) per) (per <= draw_subs: full sub-tiles of a 16-byte aligned
+// row), holds their raw vectors in registers, and publishes their totals. After one barrier
+// every warp forms the same prefix of the 16 block totals; the warp whose block holds tau
+// locates the sub-tile among its own totals and the token among its registers (the sub-tile's
+// 32 lanes x 8 elements, scanned with the pass's arithmetic). Float sums throughout (see
+// bonus_search). When rounding leaves tau at or past the chunk's end, every level follows its
+// last candidate with mass: the draw is the chunk's last token with r > 0. Returns the token
+// (-1 when the chunk has no mass); all threads call it, and it ends synchronised.
+template <int DT>
+__device__ int chunk_draw(const Ctx &c, Smem &sm, int jlo, int jhi, float tau) {
+    constexpr int K = draw_subs<DT>();
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = jhi - jlo;
+    const int per = (n + kWarps - 1) / kWarps;
+    const int a = jlo + min(warp * per, n), z = jlo + min(warp * per + per, n);
+    uint4 za[K], zb[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+        if (a + k < z) fetch<DT>(c.zrow, (a + k) * kSub + lane * 8, za[k], zb[k]);
+    float wsum = 0.f;
+    int rc = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (a + k < z) {
+            float zs[8], ds[8], r[8];
+            shifted8<DT>(za[k], zb[k], c.negm, zs);
+            residual8<DRAFT_POINT>(c, sm, zs, ds, r);
+            zero_rejected(sm, a + k, lane, rc, r);
+            float t = sum8(r);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(full, t, o);   // same in all lanes
+            if (lane == 0) sm.dsub[warp][k] = t;
+            wsum += t;
+        }
+    }
+    if (lane == 0) sm.dtot[warp] = wsum;
+    if (lane == 0 && threadIdx.x == 0) sm.bonus = -1;
+    __syncthreads();
+    // every warp: the same prefix of the block totals, and the block holding tau
+    const float bt = lane < kWarps ? sm.dtot[lane] : 0.f;
+    const float incl = warp_incl_scan(bt);
+    float excl = __shfl_up_sync(full, incl, 1);
+    if (lane == 0) excl = 0.f;
+    const unsigned hit = __ballot_sync(full, lane < kWarps && incl > tau);
+    const unsigned pos = __ballot_sync(full, lane < kWarps && bt > 0.f);
+    int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    float tr = hit ? tau : INFINITY;
+    if (warp == owner) {
+        tr -= __shfl_sync(full, excl, owner);
+        // the sub-tile: first with its running total past tr (else the last with mass)
+        int ks = -1, kl = -1;
+        float pre = 0.f, prel = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (a + k < z && ks < 0) {
+                const float t = sm.dsub[warp][k];
+                if (pre + t > tr) {
+                    ks = k;
+                } else {
+                    if (t > 0.f) {
+                        kl = k;
+                        prel = pre;
+                    }
+                    pre += t;
+                }
+            }
+        }
+        if (ks < 0) {
+            ks = kl;
+            pre = prel;
+            tr = INFINITY;
+        }
+        int tok = -1;
+        if (ks >= 0) {
+            uint4 xa = za[0], xb = zb[0];
+#pragma unroll
+            for (int k = 1; k < K; ++k)
+                if (k == ks) {
+                    xa = za[k];
+                    xb = zb[k];
+                }
+            const int js = a + ks;
+            float zs[8], ds[8], r[8];
+            int rc2 = 0;
+            shifted8<DT>(xa, xb, c.negm, zs);
+            residual8<DRAFT_POINT>(c, sm, zs, ds, r);
+            zero_rejected(sm, js, lane, rc2, r);
+            const float trs = tr - pre;
+            const float inc = warp_incl_scan(sum8(r));
+            float exf = __shfl_up_sync(full, inc, 1);
+            if (lane == 0) exf = 0.f;
+            int lastk = -1;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) lastk = r[q] > 0.f ? js * kSub + lane * 8 + q : lastk;
+            const unsigned b2 = __ballot_sync(full, inc > trs);
+            if (b2 != 0) {
+                const int l = __ffs(b2) - 1;
+                if (lane == l) {
+                    float part = exf;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        part += r[q];
+                        if (tok < 0 && r[q] > 0.f && part > trs) tok = js * kSub + lane * 8 + q;
+                    }
+                    if (tok < 0) tok = lastk;
+                }
+                tok = __shfl_sync(full, tok, l);
+            }
+            if (tok < 0) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lastk = max(lastk, shfl_xor(lastk, o));
+                tok = lastk;
+            }
+        }
+        if (lane == 0) sm.bonus = tok;
+    }
+    __syncthreads();
+    return sm.bonus;
+}
+
 // ---- the walk (warp 0) ---------------------------------------------------------------------
 
 struct WalkState {
@@ -582,6 +718,53 @@ struct WalkState {
     bool entering, just_summed;
     bool stats_ready;          // lazy walks: the current node's statistics are in shared memory
 };
+
+// Point drafts, on entering a node whose children are all among nodes 1..31: every child's
+// test at once instead of one child per step (warp 0; lane i holds node i). Children are
+// visited in ascending node index; a child repeating an earlier sibling's token is rejected
+// outright (that token is already rejected); for the others, the rejected mass before child c
+// is the sum of e_t over the distinct tokens of the earlier siblings (a float64 warp scan in
+// node order), and c is accepted iff u[c] (S - that mass) < e_t(c), the step-by-step rule. The
+// sweep stops at the first child that is accepted or whose denominator fell below S / 16 (the
+// exact re-sum then runs first, as in the step-by-step walk). The tokens of the children
+// before it enter the rejected list R (ascending, with their e_t) and their mass w.sub.
+// Returns the accepted child, or -1 with w.kids holding the children not tested yet.
+__device__ int sibling_sweep(WalkState &w, Smem &sm) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const unsigned kids = (unsigned)w.kids;
+    const bool k = (kids >> lane) & 1u;
+    const int t = k ? sm.tok[lane] : -1 - lane;   // distinct keys for non-children
+    // every lane takes part in the match (a warp-wide instruction: none may skip it)
+    const unsigned same = __match_any_sync(full, t);
+    const bool d = k && (same & ((1u << lane) - 1u)) != 0u;
+    const float f = sm.ec[lane];
+    const bool live = k && !d;
+    const double incl = warp_incl_scan_d(live ? (double)f : 0.0);
+    double x = __shfl_up_sync(full, incl, 1);   // rejected mass before this child
+    if (lane == 0) x = 0.0;
+    const double n = w.base - x;
+    const bool h = live && n < w.base * (1.0 / 16.0);
+    const bool acc = live && !h && (double)sm.u[lane] * n < (double)f;
+    const unsigned stop = __ballot_sync(full, h || acc);
+    const int first = stop ? __ffs(stop) - 1 : 32;
+    // rejected list: the distinct tokens before `first`, ranked by value
+    const bool r = live && lane < first;
+    const unsigned rl = __ballot_sync(full, r);
+    int rank = 0;
+    for (unsigned m = rl; m; m &= m - 1u) rank += __shfl_sync(full, t, __ffs(m) - 1) < t;
+    __syncwarp();
+    if (r && walk_check(rank < kMaxN, sm, DBG_WALK)) {
+        sm.R[rank] = t;
+        sm.RE[rank] = f;
+    }
+    if (lane == 0) sm.nR = __popc(rl);
+    __syncwarp();
+    w.sub = __shfl_sync(full, first < 32 ? x : incl, first < 32 ? first : 31);
+    w.kids = first < 32 ? w.kids & (~0ull << first) : 0ull;
+    const unsigned accs = __ballot_sync(full, acc);
+    return first < 32 && ((accs >> first) & 1u) ? first : -1;
+}
 
 // Advances the walk until it needs a pass over the vocabulary or ends; returns the command.
 // Executed by all lanes of warp 0 with identical state.
@@ -636,6 +819,24 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
             }
             __syncwarp();
             w.entering = false;
+            if constexpr (DK == DRAFT_POINT) {
+                if (w.kids && (w.kids >> 32) == 0ull) {
+                    const int c = sibling_sweep(w, sm);
+                    if (c > 0) {   // accepted: move to it
+                        if (!walk_check(w.L < N - 1 && c < N, sm, DBG_WALK)) {
+                            w.st = SPEC_REQ_INTERNAL;
+                            continue;
+                        }
+                        if (lane == 0) sm.path[w.L] = c;
+                        __syncwarp();
+                        w.L += 1;
+                        w.node = c;
+                        w.entering = true;
+                        w.stats_ready = false;
+                        continue;
+                    }
+                }
+            }
         }
         if (w.kids == 0) return CMD_BONUS;
         if (DK != DRAFT_POINT && sm.pending) {
@@ -728,7 +929,7 @@ __device__ int advance(WalkState &w, Smem &sm, int N) {
 // chunk's (max, sum) goes to sm.cpart, so a bonus drawn from this row sums only one chunk.
 // Results land in sm.part_out (m, s, flags). All threads call it; it ends synchronised.
 template <int DT>
-__device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
+__device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm, uint4 *ring) {
     using namespace rowpass;
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kEpv = 16 / kEsz;
@@ -749,6 +950,33 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
     if (g == 0 && gt < head) proc_scalar<ROW_SAMPLE>(a, load_elem<DT>(row, gt), gt, k);
     const uint4 *vb = reinterpret_cast<const uint4 *>(row + head * kEsz);
     int i = row_chunk_vec(g, nv, V, aligned, kEpv, kLazyChunks) + gt;
+    if (ring && aligned) {
+        // A ring of this thread's own slots: D copies in flight; each step waits for the
+        // oldest (cp.async.wait_group), takes it and refills its slot with the vector D steps
+        // ahead. The thread reads back only its own slots, so no barrier is needed, and it
+        // visits its vectors in the same order as the register loop below.
+        constexpr int D = SPEC_LAZY_RING;
+        uint4 *slots = ring + (size_t)threadIdx.x * D;
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            const int id = i + d * kGroup;
+            if (id < v1 && walk_check(id < nv, sm, DBG_INDEX)) cp_async16(slots + d, vb + id);
+            cp_async_commit();
+        }
+        for (int d = 0; i < v1; i += kGroup, d = d + 1 == D ? 0 : d + 1) {
+            cp_async_wait<D - 1>();
+            const uint4 w = slots[d];
+            const int in = i + D * kGroup;
+            if (in < v1 && walk_check(in < nv, sm, DBG_INDEX)) cp_async16(slots + d, vb + in);
+            cp_async_commit();
+            const int e0 = (int)head + i * kEpv;
+            if (DT == 1)
+                proc_bf16<ROW_SAMPLE>(a, w, e0, k);
+            else
+                proc_f32<ROW_SAMPLE>(a, w, e0, k);
+        }
+        cp_async_wait<0>();
+    }
     for (; i + (kUnroll - 1) * kGroup < v1; i += kUnroll * kGroup) {
         uint4 w[kUnroll];
 #pragma unroll
@@ -799,7 +1027,8 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm) {
 // node, of its draft row) with the same per-element arithmetic as the row-statistics
 // kernel, plus e_t at the children's tokens. All threads call it; it ends synchronised.
 template <int DT, int DK, int DDT>
-__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd) {
+__device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int nd,
+                           uint4 *ring) {
     constexpr int kEsz = DT == 1 ? 2 : 4;
     constexpr int kDDT = DK == DRAFT_LOGITS ? DDT : 0;
     constexpr int kDEsz = kDDT == 1 ? 2 : 4;
@@ -824,7 +1053,7 @@ __device__ void lazy_stats(const SampleWalkParams &P, Smem &sm, size_t base, int
         const bool kids = __any_sync(0xffffffffu, any);
         if (lane == 0) sm.haskids = kids;
     }
-    lazy_row_pass<DT>(zrow, V, k, sm);
+    lazy_row_pass<DT>(zrow, V, k, sm, ring);
     const rowpass::Part p = sm.part_out;
     if (threadIdx.x == 0) sm.cpart_node = nd;
     if (warp == 0) {
@@ -1003,7 +1232,8 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         cmd = lead<CL>(sm, sm.cmd);
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
         if (LAZY && cmd == CMD_STATS) {
-            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node);
+            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node,
+                                    reinterpret_cast<uint4 *>(subsum + lazy_ring_offset(P.V)));
             continue;
         }
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
@@ -1063,18 +1293,20 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             }
             if (q >= 0) {
                 const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                // stage the chunk when it fits and holds full sub-tiles only
-                uint4 *stage = !LAZY && jhi - jlo <= stage_subs<DT>() && jhi <= c.V / kSub
-                                   ? reinterpret_cast<uint4 *>(subsum + subsum_floats(c.V))
-                                   : nullptr;
-                residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false, stage);
-                if (warp == 0) {
-                    const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
-                                                            sm.ctau, stage);
-                    if (lane == 0) sm.bonus = v;
+                if (jhi - jlo <= kWarps * draw_subs<DT>() && jhi <= c.V / kSub) {
+                    // full sub-tiles that the warps can hold (an eighth of the row for eager
+                    // walks, a sixteenth for lazy ones): drawn without a search
+                    drawn = chunk_draw<DT>(c, sm, jlo, jhi, (float)sm.ctau) >= 0;
+                } else {
+                    residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);
+                    if (warp == 0) {
+                        const int v = bonus_search<DT, DK, DDT>(c, sm, subsum, ub, jlo, jhi,
+                                                                sm.ctau);
+                        if (lane == 0) sm.bonus = v;
+                    }
+                    __syncthreads();
+                    drawn = sm.bonus >= 0;
                 }
-                __syncthreads();
-                drawn = sm.bonus >= 0;
             }
         }
         for (int attempt = 0; attempt < 3 && !drawn; ++attempt) {
@@ -1160,15 +1392,7 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
 
 template <int DT, int DK, int DDT>
 cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
-    // sub-tile sums, then (eager point drafts) the staging area of the bonus chunk
-    const size_t stage = DK == DRAFT_POINT && !p.lazy ? (size_t)kStageBytes : 0;
-    const size_t smem = sizeof(float) * (size_t)subsum_floats(p.V) + stage;
-    if (stage) {
-        const cudaError_t e = cudaFuncSetAttribute(walk_sample_kernel<DT, DK, DDT, false>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    const size_t smem = sizeof(float) * (size_t)subsum_floats(p.V);   // sub-tile sums
     if (!p.lazy) {
         const dim3 block(kThreads);
         // Point drafts pass over one chunk of the stop row at most: a cluster's barriers would
@@ -1197,7 +1421,13 @@ cudaError_t launch_ws(const SampleWalkParams &p, cudaStream_t st) {
         return launch_dependent(walk_sample_kernel<DT, DK, DDT, false>, dim3(p.B), block, smem,
                                 st, p);
     }
-    walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, smem, st>>>(p);
+    // lazy walks: the sub-tile sums, then the ring of the row passes
+    const size_t lsmem = sizeof(float) * (size_t)lazy_ring_offset(p.V) + kLazyRingBytes;
+    const cudaError_t e = cudaFuncSetAttribute(walk_sample_kernel<DT, DK, DDT, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)lsmem);
+    if (e != cudaSuccess) return e;
+    walk_sample_kernel<DT, DK, DDT, true><<<p.B, kThreads, lsmem, st>>>(p);
     return cudaGetLastError();
 }
 

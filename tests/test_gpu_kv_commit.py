@@ -109,3 +109,52 @@ def test_kv_commit_matches_oracle(h, src, cache, layout, D, scales):
     else:
         assert np.array_equal(gk.cpu().numpy(), ref_k)
         assert np.array_equal(gv.cpu().numpy(), ref_v)
+
+
+@pytest.mark.parametrize("cache", [K.FP8_E4M3, K.FP8_E5M2])
+def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
+    """The fp8 encoding of x / scale near every fp8 rounding boundary: quotients placed on the
+    midpoints between adjacent fp8 values (ties to even), a few float32 steps either side of
+    them, beyond the largest finite value (saturation) and under the smallest subnormal (zero),
+    for scales that are not powers of two. These are the cases where the library's reciprocal shortcut must defer to the
+    correctly rounded division; the cache must equal the oracle's encoding bit for bit."""
+    rng = np.random.default_rng(90 + cache)
+    vals = K._fp8_table(cache)[:0x7F]
+    vals = np.sort(vals[np.isfinite(vals)])
+    mids = (vals[1:] + vals[:-1]) / 2
+    mids = np.concatenate([mids, [vals[-1] * 1.0625, vals[-1] * 4.0]])      # saturation
+    least = vals[vals > 0][0]          # quotients under the smallest subnormal, down to zero
+    mids = np.concatenate([mids, least * np.array([0.3, 0.2, 0.126, 0.124, 0.1, 1e-3]),
+                           [1e-30, 1e-40]])
+    t = mids.astype(np.float32)
+    steps = (t.view(np.int32)[:, None] + np.arange(-3, 4, dtype=np.int32)[None, :]).ravel()
+    t = steps.astype(np.int32).view(np.float32)
+    t = np.concatenate([t, -t, np.float32([0.0, -0.0])])   # and zeros of both signs
+    B, N, H, D = 4, 8, 2, 64
+    per = H * D
+    slots = B * N
+    total = slots * per
+    t = np.resize(rng.permutation(t), total).astype(np.float32)
+    scale = (2.0 ** rng.uniform(-4, 4, (B, N)) * rng.uniform(1.01, 1.99, (B, N))).astype(
+        np.float32)
+    x = (t.reshape(B, N, H, D) * scale[:, :, None, None]).astype(np.float32)
+    kv = np.tile(np.arange(N, dtype=np.int32), (B, 1))        # every node committed
+    al = np.full(B, N - 1, np.int32)
+    bs, max_blocks = 8, 1
+    table = np.arange(B, dtype=np.int32).reshape(B, 1)
+    pos = np.zeros(B, np.int32)
+    shape = (B, bs, H, D)
+    ck0 = torch.zeros(shape, dtype=torch.uint8)
+    ref_k, ref_v, ref_st = K.kv_commit(x, x, kv, al, ck0.numpy(), ck0.numpy(), K.NHD, bs, table,
+                                       pos, cache_kind=cache, k_scale=scale, v_scale=scale)
+    gk, gv = ck0.to(DEV), ck0.clone().to(DEV)
+    tx = torch.from_numpy(x).to(DEV)
+    st = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    sc = torch.from_numpy(scale).to(DEV)
+    G.spec_kv_commit(h, tx, tx, torch.from_numpy(kv).to(DEV), torch.from_numpy(al).to(DEV), gk,
+                     gv, K.NHD, torch.from_numpy(table).to(DEV), torch.from_numpy(pos).to(DEV),
+                     cache_kind=cache, k_scale=sc, v_scale=sc, commit_status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().numpy().tolist() == ref_st.tolist() == [0] * B
+    assert np.array_equal(gk.cpu().numpy(), ref_k)
+    assert np.array_equal(gv.cpu().numpy(), ref_v)
