@@ -781,12 +781,15 @@ def bench_kv_commit(h, dev, stream, args):
     pos = torch.full((B,), 37, dtype=torch.int32, device=dev)
     flush = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
-    for name, cache_kind, esz in (("bf16", G.SPEC_CACHE_SAME, 2), ("fp8_e4m3",
-                                                                   G.SPEC_CACHE_FP8_E4M3, 1)):
+    # fp8 caches: a power-of-two scale (one multiply per element), and a scale that is not one
+    # (the reciprocal route with its rounding-boundary test)
+    for name, cache_kind, esz, sv in (("bf16", G.SPEC_CACHE_SAME, 2, None),
+                                      ("fp8_e4m3", G.SPEC_CACHE_FP8_E4M3, 1, 0.5),
+                                      ("fp8_e4m3_scale_0.0173", G.SPEC_CACHE_FP8_E4M3, 1, 0.0173)):
         cdt = torch.bfloat16 if esz == 2 else torch.uint8
         ck = torch.zeros((B * max_blocks, bs, H, D), dtype=cdt, device=dev)
         cv = torch.zeros_like(ck)
-        scale = torch.tensor([0.5], device=dev) if esz == 1 else None
+        scale = torch.tensor([sv], device=dev) if sv is not None else None
 
         def call():
             G.spec_kv_commit(h, src_k, src_v, kv, al, ck, cv, G.SPEC_KV_NHD, table, pos,
@@ -796,7 +799,8 @@ def bench_kv_commit(h, dev, stream, args):
         moved = B * (L + 1) * 2 * H * D * (2 + esz)   # read K and V, write them into the cache
         out[name] = {"ms_per_call": ms, "bytes": moved, **_hbm(moved, ms)}
     out["config"] = ("B=256 N=64, 8 slots per request, H=32 D=128 bf16 sources, NHD cache of "
-                     "16-token blocks; L2 flushed before every call")
+                     "16-token blocks; fp8 per-tensor scale 0.5 or 0.0173; L2 flushed before "
+                     "every call")
     return out
 
 

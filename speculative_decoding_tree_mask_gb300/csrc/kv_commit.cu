@@ -110,16 +110,51 @@ __device__ __forceinline__ float fp8_quotient(float x, float s, float y, bool &o
 // The correctly rounded division, kept out of line: it runs for a few elements in a million.
 __device__ __noinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
 
-// Whether a scale allows the reciprocal route (its reciprocal is a normal float).
-__device__ __forceinline__ bool recip_ok(float s) {
+// The common cases of fp8_quotient, cheaply: q1 (same steps) in the fp8 normal binades with its
+// dropped mantissa bits more than two steps from the midpoint pattern, or q1 nonzero, finite and
+// exact (zero residual). The exact case matters: a 16-bit source over a power-of-two scale lands
+// exactly on an fp8 midpoint for one element in 16 (e4m3), and sending those elements to the
+// full path would make nearly every warp take it. Elements that fail this test take
+// fp8_quotient_full (zeros, the subnormal range, saturation, inexact near-ties, non-finite).
+template <int CACHE>
+__device__ __forceinline__ float fp8_q1(float x, float s, float y) {
+    const float q0 = x * y;
+    return fmaf(fmaf(-q0, s, x), y, q0);
+}
+template <int CACHE>
+__device__ __forceinline__ bool fp8_fast_ok(float q1, float x, float s) {
+    constexpr int KB = CACHE == 1 ? 3 : 2;
+    constexpr int EMIN = CACHE == 1 ? -6 : -14;
+    constexpr int EMAX = CACHE == 1 ? 8 : 15;
+    constexpr uint32_t LO = uint32_t(127 + EMIN) << 23, RANGE = uint32_t(EMAX - EMIN + 1) << 23;
+    constexpr uint32_t DROP = (1u << (23 - KB)) - 1u, HALF = 1u << (22 - KB);
+    const uint32_t mag = __float_as_uint(q1) & 0x7fffffffu;
+    return (mag - LO < RANGE && (mag & DROP) - HALF + 2u > 4u) ||
+           (mag - 1u < 0x7f7fffffu && fmaf(-q1, s, x) == 0.f);
+}
+template <int CACHE>
+__device__ __noinline__ float fp8_quotient_full(float x, float s, float y, bool fast) {
+    bool ok = false;
+    const float q = fast ? fp8_quotient<CACHE>(x, s, y, ok) : 0.f;
+    return ok ? q : div_rn(x, s);
+}
+
+// How a scale's quotients are formed: a power-of-two scale (its reciprocal exact, so
+// x * RN(1/s) is the same real number as x / s and rounds alike: one multiply, no test), a
+// scale with a normal reciprocal (fp8_q1 and fp8_fast_ok, then fp8_quotient_full), or the
+// correctly rounded division for every element.
+enum { Q_POW2 = 0, Q_RECIP = 1, Q_DIV = 2 };
+__device__ __forceinline__ int scale_mode(float s) {
+    const uint32_t u = __float_as_uint(s) & 0x7fffffffu;
+    if ((u & 0x7fffffu) == 0u && u >= 0x00800000u && u <= 0x7e800000u) return Q_POW2;
     const float a = fabsf(s);
-    return a >= 1e-37f && a <= 1e37f;
+    return a >= 1e-37f && a <= 1e37f ? Q_RECIP : Q_DIV;
 }
 
 // One element src[si] -> cache[di] (the unvectorised path).
 template <int SRC, int CACHE>
 __device__ __forceinline__ void put1(const void *src, size_t si, void *dst, size_t di,
-                                     float scale, float rcp, bool fast) {
+                                     float scale, float rcp, int mode) {
     if (CACHE == 0) {
         if (SRC == 0)
             reinterpret_cast<float *>(dst)[di] = __ldg(reinterpret_cast<const float *>(src) + si);
@@ -128,10 +163,8 @@ __device__ __forceinline__ void put1(const void *src, size_t si, void *dst, size
                 __ldg(reinterpret_cast<const unsigned short *>(src) + si);
     } else {
         const float x = src_elem<SRC>(src, si);
-        bool ok = false;
-        float q = fast ? fp8_quotient<CACHE>(x, scale, rcp, ok) : 0.f;
-        if (!ok) q = div_rn(x, scale);
-        reinterpret_cast<uint8_t *>(dst)[di] = (uint8_t)fp8_of<CACHE>(q);
+        reinterpret_cast<uint8_t *>(dst)[di] = (uint8_t)fp8_of<CACHE>(
+            mode == Q_POW2 ? x * rcp : fp8_quotient_full<CACHE>(x, scale, rcp, mode == Q_RECIP));
     }
 }
 
@@ -152,7 +185,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // at cache element di.
 template <int SRC, int CACHE>
 __device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, float scale,
-                                       float rcp, bool fast) {
+                                       float rcp, int mode) {
     if (CACHE == 0) {
         uint4 *dp = reinterpret_cast<uint4 *>(reinterpret_cast<char *>(dst) +
                                               di * (size_t)src_bytes<SRC>());
@@ -184,24 +217,29 @@ __device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, f
         }
     }
     float q[8];
-    unsigned slow = 0;
+    if (mode == Q_POW2) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        bool ok = false;
-        q[i] = fast ? fp8_quotient<CACHE>(x[i], scale, rcp, ok) : 0.f;
-        slow |= ok ? 0u : 1u << i;
-    }
-    if (slow) {
+        for (int i = 0; i < 8; ++i) q[i] = x[i] * rcp;
+    } else {
+        unsigned slow = mode == Q_RECIP ? 0u : 0xffu;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (slow & (1u << i)) q[i] = div_rn(x[i], scale);
+        for (int i = 0; i < 8; ++i) {
+            q[i] = fp8_q1<CACHE>(x[i], scale, rcp);
+            slow |= fp8_fast_ok<CACHE>(q[i], x[i], scale) ? 0u : 1u << i;
+        }
+        if (slow) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (slow & (1u << i))
+                    q[i] = fp8_quotient_full<CACHE>(x[i], scale, rcp, mode == Q_RECIP);
+        }
     }
-    // the magnitudes in pairs (one conversion per two elements), the signs set apart: the
-    // conversion gives +0 for a negative value that rounds to zero, the format keeps -0
+    // pairs (one conversion per two elements) with the signs OR'd in: the conversion gives +0
+    // for a negative value that rounds to zero, the format keeps -0
     uint32_t c[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        c[i] = fp8x2(fabsf(q[2 * i]), fabsf(q[2 * i + 1]), CACHE) |
+        c[i] = fp8x2(q[2 * i], q[2 * i + 1], CACHE) |
                ((__float_as_uint(q[2 * i]) >> 24) & 0x80u) |
                ((__float_as_uint(q[2 * i + 1]) >> 16) & 0x8000u);
         if (q[2 * i] != q[2 * i]) c[i] = (c[i] & 0xff00u) | 0x7fu;           // NaN: 0x7F
@@ -272,7 +310,7 @@ struct Unit {
 };
 
 template <int SRC, int CACHE, bool VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     kv_commit_kernel(KvCommitParams P, int pieces, int cached) {
     // dynamic shared memory: [staging: K then V rows of one unit][2][B] (last slot, position)
     extern __shared__ __align__(16) unsigned char smem[];
@@ -406,8 +444,9 @@ __global__ void __launch_bounds__(kThreads)
         const int nnode = un < units ? __ldg(P.kv_commit + (size_t)nxt.b * N + nxt.j) : -1;
         const bool live = src_ok && blk >= 0 && blk < P.num_blocks;
         const int off = live ? p - bi * P.block_size : 0;
-        const bool kfast = CACHE && recip_ok(ks), vfast = CACHE && recip_ok(vs);
-        const float krcp = kfast ? __frcp_rn(ks) : 1.f, vrcp = vfast ? __frcp_rn(vs) : 1.f;
+        const int kmode = CACHE ? scale_mode(ks) : Q_DIV, vmode = CACHE ? scale_mode(vs) : Q_DIV;
+        const float krcp = kmode != Q_DIV ? __frcp_rn(ks) : 1.f;
+        const float vrcp = vmode != Q_DIV ? __frcp_rn(vs) : 1.f;
         if (VEC) {
             if (src_ok) cp_async_wait_all();   // this thread's own copies
 #pragma unroll
@@ -417,16 +456,16 @@ __global__ void __launch_bounds__(kThreads)
                     kv_index_ok(P, b, sbase + e, cache_index(P, blk, off, e), 8)) {
                     const size_t di = cache_index(P, blk, off, e);
                     const int sl = (tid + q * kThreads) * (SRC == 0 ? 2 : 1);
-                    store8<SRC, CACHE>(stage_k + sl, P.cache_k, di, ks, krcp, kfast);
-                    store8<SRC, CACHE>(stage_v + sl, P.cache_v, di, vs, vrcp, vfast);
+                    store8<SRC, CACHE>(stage_k + sl, P.cache_k, di, ks, krcp, kmode);
+                    store8<SRC, CACHE>(stage_v + sl, P.cache_v, di, vs, vrcp, vmode);
                 }
             }
         } else {
             for (int e = e0 + tid; live && e < e1; e += kThreads) {
                 const size_t di = cache_index(P, blk, off, e);
                 if (!kv_index_ok(P, b, sbase + e, di, 1)) continue;
-                put1<SRC, CACHE>(P.src_k, sbase + e, P.cache_k, di, ks, krcp, kfast);
-                put1<SRC, CACHE>(P.src_v, sbase + e, P.cache_v, di, vs, vrcp, vfast);
+                put1<SRC, CACHE>(P.src_k, sbase + e, P.cache_k, di, ks, krcp, kmode);
+                put1<SRC, CACHE>(P.src_v, sbase + e, P.cache_v, di, vs, vrcp, vmode);
             }
         }
         u = un;

@@ -53,10 +53,12 @@ namespace {
 #define SPEC_LAZY_UNROLL 2   // 16-byte loads in flight per thread in the lazy row pass (rows that are not 16-byte aligned)
 #endif
 // Lazy row passes over 16-byte aligned rows stage their loads through a ring of cp.async
-// copies in shared memory instead: SPEC_LAZY_RING vectors in flight per thread (80 KiB per
-// CTA), twice the register loads, without holding registers.
+// copies in shared memory instead: SPEC_LAZY_RING vectors in flight per thread (32 KiB per
+// CTA), twice the register loads, without holding registers. Measured on the large tree (lazy
+// sampling call): 45.5 us without the ring, 34.9 us with 4 or 6 slots, 35.3 us with 10; at
+// mean accept length 1.41, 120 / 99.9 / 100.8 / 107 us.
 #ifndef SPEC_LAZY_RING
-#define SPEC_LAZY_RING 10
+#define SPEC_LAZY_RING 4
 #endif
 
 constexpr int kThreads = 512;
@@ -172,6 +174,25 @@ __device__ __forceinline__ void fetch(const char *row, int e0, uint4 &a, uint4 &
         a = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4);
         b = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4 + 1);
     }
+}
+
+// fetch, skipping the vectors that start at or past `lim` (they read as zeros).
+template <int DT>
+__device__ __forceinline__ void fetch_below(const char *row, int e0, int lim, uint4 &a, uint4 &b) {
+    a = b = make_uint4(0u, 0u, 0u, 0u);
+    if (DT == 1) {
+        if (e0 < lim) a = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 8);
+    } else {
+        if (e0 < lim) a = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4);
+        if (e0 + 4 < lim) b = ldg_stream(reinterpret_cast<const uint4 *>(row) + e0 / 4 + 1);
+    }
+}
+
+// No mass for the elements e0 + q at or past V.
+__device__ __forceinline__ void mask_past(float (&r)[8], int e0, int V) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (e0 + q >= V) r[q] = 0.f;
 }
 
 // x[q] = value(e0 + q) + c for 8 elements held in one (bf16) or two (f32) 16-byte vectors.
@@ -583,8 +604,9 @@ __device__ void chunk_marks(const Ctx &c, Smem &sm, const float2 *part, int nc) 
 
 // Point drafts: the bonus token for tau (relative to the start of the chunk's sub-tiles
 // [jlo, jhi)), drawn without a search by one warp. Warp w streams the contiguous sub-tiles
-// [jlo + w per, jlo + (w + 1) per) (per <= draw_subs: full sub-tiles of a 16-byte aligned
-// row), holds their raw vectors in registers, and publishes their totals. After one barrier
+// [jlo + w per, jlo + (w + 1) per) (per <= draw_subs sub-tiles of a 16-byte aligned row),
+// holds their raw vectors in registers, and publishes their totals; in the row's ragged last
+// sub-tile (V a multiple of the vector width) the vectors past V are skipped. After one barrier
 // every warp forms the same prefix of the 16 block totals; the warp whose block holds tau
 // locates the sub-tile among its own totals and the token among its registers (the sub-tile's
 // 32 lanes x 8 elements, scanned with the pass's arithmetic). Float sums throughout (see
@@ -599,10 +621,14 @@ __device__ int chunk_draw(const Ctx &c, Smem &sm, int jlo, int jhi, float tau) {
     const int n = jhi - jlo;
     const int per = (n + kWarps - 1) / kWarps;
     const int a = jlo + min(warp * per, n), z = jlo + min(warp * per + per, n);
+    // The row's ragged last sub-tile (V a multiple of the vector width here): vectors at or
+    // past V are not loaded and their elements get no mass. `ragged` is warp-uniform.
+    const bool ragged = z * kSub > c.V;
     uint4 za[K], zb[K];
 #pragma unroll
     for (int k = 0; k < K; ++k)
-        if (a + k < z) fetch<DT>(c.zrow, (a + k) * kSub + lane * 8, za[k], zb[k]);
+        if (a + k < z) fetch_below<DT>(c.zrow, (a + k) * kSub + lane * 8, ragged ? c.V : INT_MAX,
+                                       za[k], zb[k]);
     float wsum = 0.f;
     int rc = 0;
 #pragma unroll
@@ -612,6 +638,7 @@ __device__ int chunk_draw(const Ctx &c, Smem &sm, int jlo, int jhi, float tau) {
             shifted8<DT>(za[k], zb[k], c.negm, zs);
             residual8<DRAFT_POINT>(c, sm, zs, ds, r);
             zero_rejected(sm, a + k, lane, rc, r);
+            if (ragged) mask_past(r, (a + k) * kSub + lane * 8, c.V);
             float t = sum8(r);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(full, t, o);   // same in all lanes
@@ -671,6 +698,7 @@ __device__ int chunk_draw(const Ctx &c, Smem &sm, int jlo, int jhi, float tau) {
             shifted8<DT>(xa, xb, c.negm, zs);
             residual8<DRAFT_POINT>(c, sm, zs, ds, r);
             zero_rejected(sm, js, lane, rc2, r);
+            if (ragged) mask_past(r, js * kSub + lane * 8, c.V);
             const float trs = tr - pre;
             const float inc = warp_incl_scan(sum8(r));
             float exf = __shfl_up_sync(full, inc, 1);
@@ -950,24 +978,27 @@ __device__ void lazy_row_pass(const char *row, int64_t V, float k, Smem &sm, uin
     if (g == 0 && gt < head) proc_scalar<ROW_SAMPLE>(a, load_elem<DT>(row, gt), gt, k);
     const uint4 *vb = reinterpret_cast<const uint4 *>(row + head * kEsz);
     int i = row_chunk_vec(g, nv, V, aligned, kEpv, kLazyChunks) + gt;
-    if (ring && aligned) {
+    constexpr int D = SPEC_LAZY_RING;
+    if (D > 0 && ring && aligned) {
         // A ring of this thread's own slots: D copies in flight; each step waits for the
         // oldest (cp.async.wait_group), takes it and refills its slot with the vector D steps
         // ahead. The thread reads back only its own slots, so no barrier is needed, and it
-        // visits its vectors in the same order as the register loop below.
-        constexpr int D = SPEC_LAZY_RING;
-        uint4 *slots = ring + (size_t)threadIdx.x * D;
+        // visits its vectors in the same order as the register loop below. Slot d of thread t
+        // sits at d * kThreads + t, so a warp's 16-byte accesses fall in distinct banks.
+        uint4 *slots = ring + threadIdx.x;
 #pragma unroll
         for (int d = 0; d < D; ++d) {
             const int id = i + d * kGroup;
-            if (id < v1 && walk_check(id < nv, sm, DBG_INDEX)) cp_async16(slots + d, vb + id);
+            if (id < v1 && walk_check(id < nv, sm, DBG_INDEX))
+                cp_async16(slots + d * kThreads, vb + id);
             cp_async_commit();
         }
         for (int d = 0; i < v1; i += kGroup, d = d + 1 == D ? 0 : d + 1) {
-            cp_async_wait<D - 1>();
-            const uint4 w = slots[d];
+            cp_async_wait<(D > 0 ? D - 1 : 0)>();
+            const uint4 w = slots[d * kThreads];
             const int in = i + D * kGroup;
-            if (in < v1 && walk_check(in < nv, sm, DBG_INDEX)) cp_async16(slots + d, vb + in);
+            if (in < v1 && walk_check(in < nv, sm, DBG_INDEX))
+                cp_async16(slots + d * kThreads, vb + in);
             cp_async_commit();
             const int e0 = (int)head + i * kEpv;
             if (DT == 1)
@@ -1293,9 +1324,11 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
             }
             if (q >= 0) {
                 const int jlo = row_chunk_sub(q, c.V, nc), jhi = row_chunk_sub(q + 1, c.V, nc);
-                if (jhi - jlo <= kWarps * draw_subs<DT>() && jhi <= c.V / kSub) {
-                    // full sub-tiles that the warps can hold (an eighth of the row for eager
-                    // walks, a sixteenth for lazy ones): drawn without a search
+                if (jhi - jlo <= kWarps * draw_subs<DT>() &&
+                    (jhi <= c.V / kSub || c.V % (DT == 1 ? 8 : 4) == 0)) {
+                    // sub-tiles that the warps can hold (an eighth of the row for eager walks,
+                    // a sixteenth for lazy ones; the last may be ragged): drawn without a
+                    // search
                     drawn = chunk_draw<DT>(c, sm, jlo, jhi, (float)sm.ctau) >= 0;
                 } else {
                     residual_pass<DT, DK, DDT>(c, sm, subsum, jlo, jhi, false);

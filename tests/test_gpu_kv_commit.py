@@ -116,7 +116,8 @@ def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
     """The fp8 encoding of x / scale near every fp8 rounding boundary: quotients placed on the
     midpoints between adjacent fp8 values (ties to even), a few float32 steps either side of
     them, beyond the largest finite value (saturation) and under the smallest subnormal (zero),
-    for scales that are not powers of two. These are the cases where the library's reciprocal shortcut must defer to the
+    for scales that are powers of two (the quotients land on the midpoints exactly) and scales
+    that are not. These are the cases where the library's reciprocal shortcut must defer to the
     correctly rounded division; the cache must equal the oracle's encoding bit for bit."""
     rng = np.random.default_rng(90 + cache)
     vals = K._fp8_table(cache)[:0x7F]
@@ -137,6 +138,7 @@ def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
     t = np.resize(rng.permutation(t), total).astype(np.float32)
     scale = (2.0 ** rng.uniform(-4, 4, (B, N)) * rng.uniform(1.01, 1.99, (B, N))).astype(
         np.float32)
+    scale[:, ::2] = 2.0 ** rng.integers(-4, 5, (B, N // 2))   # powers of two: exact ties
     x = (t.reshape(B, N, H, D) * scale[:, :, None, None]).astype(np.float32)
     kv = np.tile(np.arange(N, dtype=np.int32), (B, 1))        # every node committed
     al = np.full(B, N - 1, np.int32)
