@@ -110,27 +110,25 @@ __device__ __forceinline__ float fp8_quotient(float x, float s, float y, bool &o
 // The correctly rounded division, kept out of line: it runs for a few elements in a million.
 __device__ __noinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
 
-// The common cases of fp8_quotient, cheaply: q1 (same steps) in the fp8 normal binades with its
-// dropped mantissa bits more than two steps from the midpoint pattern, or q1 nonzero, finite and
-// exact (zero residual). The exact case matters: a 16-bit source over a power-of-two scale lands
-// exactly on an fp8 midpoint for one element in 16 (e4m3), and sending those elements to the
-// full path would make nearly every warp take it. Elements that fail this test take
-// fp8_quotient_full (zeros, the subnormal range, saturation, inexact near-ties, non-finite).
+// The common case of fp8_quotient, cheaply: q1 (same steps) in the fp8 normal binades with its
+// dropped mantissa bits more than two steps from the midpoint pattern. Elements that fail this
+// test take fp8_quotient_full (zeros, the subnormal range, saturation, near-ties, exact
+// quotients, non-finite). Power-of-two scales, whose quotients are exact and land on fp8
+// midpoints often (one 16-bit source value in 16 for e4m3), never come here.
 template <int CACHE>
 __device__ __forceinline__ float fp8_q1(float x, float s, float y) {
     const float q0 = x * y;
     return fmaf(fmaf(-q0, s, x), y, q0);
 }
 template <int CACHE>
-__device__ __forceinline__ bool fp8_fast_ok(float q1, float x, float s) {
+__device__ __forceinline__ bool fp8_fast_ok(float q1) {
     constexpr int KB = CACHE == 1 ? 3 : 2;
     constexpr int EMIN = CACHE == 1 ? -6 : -14;
     constexpr int EMAX = CACHE == 1 ? 8 : 15;
     constexpr uint32_t LO = uint32_t(127 + EMIN) << 23, RANGE = uint32_t(EMAX - EMIN + 1) << 23;
     constexpr uint32_t DROP = (1u << (23 - KB)) - 1u, HALF = 1u << (22 - KB);
     const uint32_t mag = __float_as_uint(q1) & 0x7fffffffu;
-    return (mag - LO < RANGE && (mag & DROP) - HALF + 2u > 4u) ||
-           (mag - 1u < 0x7f7fffffu && fmaf(-q1, s, x) == 0.f);
+    return mag - LO < RANGE && (mag & DROP) - HALF + 2u > 4u;
 }
 template <int CACHE>
 __device__ __noinline__ float fp8_quotient_full(float x, float s, float y, bool fast) {
@@ -225,7 +223,7 @@ __device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, f
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             q[i] = fp8_q1<CACHE>(x[i], scale, rcp);
-            slow |= fp8_fast_ok<CACHE>(q[i], x[i], scale) ? 0u : 1u << i;
+            slow |= fp8_fast_ok<CACHE>(q[i]) ? 0u : 1u << i;
         }
         if (slow) {
 #pragma unroll
