@@ -629,21 +629,38 @@ __device__ int chunk_draw(const Ctx &c, Smem &sm, int jlo, int jhi, float tau) {
     for (int k = 0; k < K; ++k)
         if (a + k < z) fetch_below<DT>(c.zrow, (a + k) * kSub + lane * 8, ragged ? c.V : INT_MAX,
                                        za[k], zb[k]);
-    float wsum = 0.f;
+    // Rejected tokens inside this warp's block are rare: test the whole block once, and zero
+    // them per sub-tile only then.
+    bool anyR = false;
+    for (int i = lane; i < sm.nR; i += 32) anyR |= sm.R[i] >= a * kSub && sm.R[i] < z * kSub;
+    anyR = __any_sync(full, anyR);
+    // The lane sums of all sub-tiles first, then their butterflies level by level, so that the
+    // K reductions overlap instead of running one after another (same sums, same order).
+    float t[K];
     int rc = 0;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
+        t[k] = 0.f;
         if (a + k < z) {
             float zs[8], ds[8], r[8];
             shifted8<DT>(za[k], zb[k], c.negm, zs);
             residual8<DRAFT_POINT>(c, sm, zs, ds, r);
-            zero_rejected(sm, a + k, lane, rc, r);
+            if (anyR) zero_rejected(sm, a + k, lane, rc, r);
             if (ragged) mask_past(r, (a + k) * kSub + lane * 8, c.V);
-            float t = sum8(r);
+            t[k] = sum8(r);
+        }
+    }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(full, t, o);   // same in all lanes
-            if (lane == 0) sm.dsub[warp][k] = t;
-            wsum += t;
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) t[k] += __shfl_xor_sync(full, t[k], o);   // same in all lanes
+    }
+    float wsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (a + k < z) {
+            if (lane == 0) sm.dsub[warp][k] = t[k];
+            wsum += t[k];
         }
     }
     if (lane == 0) sm.dtot[warp] = wsum;
