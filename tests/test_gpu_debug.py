@@ -114,6 +114,7 @@ def test_kv_commit_case(h):
     from oracle import kv_commit as KO
     K.test_kv_commit_matches_oracle(h, "bf16", KO.FP8_E4M3, KO.HND, 128, "token")
     K.test_kv_commit_matches_oracle(h, "f32", KO.SAME, KO.NHD, 36, "tensor")
+    K.test_kv_commit_fp8_quotients_at_rounding_boundaries(h, KO.FP8_E4M3)
 
 
 def test_no_allocation_call(orc, dbg_lib):

@@ -218,6 +218,33 @@ def test_sample_point_trie(h, orc, T, boost):
     PY.compare_sample(gpu, ref)
 
 
+@pytest.mark.parametrize("lazy", [False, True])
+@pytest.mark.parametrize("dtype,V", [("bf16", 20008), ("bf16", 151936), ("f32", 4100),
+                                     ("bf16", 20001)])
+def test_bonus_in_the_ragged_last_chunk(h, orc, dtype, V, lazy):
+    """Bonus uniforms near 1 put tau in the row's last chunk, whose last 256-token sub-tile is
+    ragged (V not a multiple of 256). The register draw takes it with the vectors past V
+    masked when V is a multiple of the vector width (8 bf16, 4 f32); V = 20001 leaves the rows
+    unaligned and takes the whole-row search instead."""
+    w = W.WORKLOADS["sampling_trie"].scaled(B=24, N=16, V=V, dtype=dtype, boost=4.0,
+                                            sigma=2.0, temperature=1.0, seed=V + 17 * lazy)
+    x = W.make(w, device=DEV)
+    u = x["uniforms"].clone()
+    u[:, w.N] = torch.linspace(0.95, 0.99999, w.B, device=DEV)
+    fn = G.verify_sample_lazy if lazy else G.verify_sample
+    gpu = PY.to_np(fn(h, x["logits"], x["draft_token"], x["parent"], 1.0, u))
+    torch.cuda.synchronize()
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], 1.0, u)
+    PY.compare_sample(gpu, ref)
+    ok = gpu["status"] == 0
+    assert ok.all()
+    # the draws land in the last chunk's tokens (an eighth of the row's sub-tiles, a sixteenth
+    # for the lazy walk's chunks)
+    nsub, nc = (V + 255) // 256, 16 if lazy else 8
+    last = nsub * (nc - 1) // nc * 256
+    assert (gpu["bonus"][ok] >= last).mean() > 0.3
+
+
 def test_sample_point_many_small_requests(h, orc):
     w = W.WORKLOADS["sampling_trie"].scaled(B=256, N=24, V=3001, dtype="f32", boost=6.0,
                                             sigma=1.5, temperature=1.0, seed=9)
