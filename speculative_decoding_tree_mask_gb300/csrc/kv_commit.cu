@@ -14,16 +14,17 @@
 //
 // Work is split into units of (slot j, request b, piece of 4096 of the slot's H*D elements),
 // ordered slot-major, so that the slots every request commits (j <= accept_len) come first.
-// A grid of up to 12 CTAs per SM strides over the units. Each CTA first reads every request's
-// accepted length and position into shared memory and stops at the deepest accepted slot of
-// the batch, so no CTA works on a slot nobody commits; the node of its first unit is loaded in
-// the same round trip. The copy is staged through shared memory with cp.async: each thread
-// copies its own 16-byte vectors of the unit's K and V rows there, waits for its own copies
-// (cp.async.wait_group: a hardware wait on the thread's own group, no spinning) and stores
-// them to the cache, so the data occupies no registers and twelve CTAs fit on an SM. A unit
-// costs two round trips: its node (loaded with the previous unit's data) starts the copies,
-// and its cache block is loaded while they are in flight. The statuses are checked by the
-// CTAs that get the fewest units.
+// A grid of one wave of CTAs (the occupancy query decides: 8 to 10 per SM, registers bound it)
+// strides over the units. Each CTA first reads every request's accepted length and position
+// into shared memory and stops at the deepest accepted slot of the batch, so no CTA works on a
+// slot nobody commits; the node of its first unit is loaded in the same round trip. The copy
+// is staged through shared memory with cp.async: each thread copies its own 16-byte vectors of
+// the unit's K and V rows there, waits for its own copies (cp.async.wait_group: a hardware wait
+// on the thread's own group, no spinning) and stores them to the cache, so the data occupies
+// no registers (holding it in registers allowed 6 CTAs per SM). A unit costs two round trips:
+// its node (loaded with the previous unit's data) starts the copies, and its cache block is
+// loaded while they are in flight. The statuses are checked by the CTAs that get the fewest
+// units.
 
 #include <cfloat>
 #include <cuda_fp16.h>
@@ -37,7 +38,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kVecs = 4;                          // 8-element vectors per thread per unit
 constexpr int kUnitElems = kThreads * 8 * kVecs;  // elements of K (and of V) per unit
-constexpr int kCtasPerSm = 12;                    // 16-bit sources: 16 KiB of staging per CTA
+constexpr int kCtasPerSm = 12;   // at most (16 KiB of staging per CTA for 16-bit sources)
 constexpr int kSmemRequests = 1024;               // requests whose (L, position) fit in smem
 
 template <int SRC>
