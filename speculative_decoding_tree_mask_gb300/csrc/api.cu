@@ -102,6 +102,16 @@ size_t esize(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
 // host memory that the device reaches at the same address (read over the host link).
 // Anything else (another GPU's memory, pageable host memory, a registration mapped at
 // another address) is refused.
+// Whether p is host memory the device can read (pinned and mapped).
+bool host_memory(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
 bool readable_by_device(const void *p, int device) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -535,6 +545,7 @@ int spec_verify_sample_lazy(spec_handle h, const void *logits, int dtype, int B,
     wp.draft_dtype = draft_dtype;
     wp.draft = draft;
     wp.lazy = 1;
+    wp.host_rows = host_memory(logits);
     wp.out = outputs(accept_len, out_tokens, kv_commit, bonus, status);
     wp.n_active = h->n_active;
     wp.dbg = h->dbg;

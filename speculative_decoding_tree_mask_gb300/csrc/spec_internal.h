@@ -206,6 +206,7 @@ struct SampleWalkParams {
     const float *mq, *sq, *qc;
     const int32_t *dflags;
     int lazy;                     // 1: no row statistics precomputed; stream visited rows only
+    int host_rows = 0;            // lazy: the logits are in host memory (read over the link)
     WalkOutputs out;
     const int32_t *n_active = nullptr;
     const float2 *chunk = nullptr;   // row-chunk partials of the target rows (eager, may be null)

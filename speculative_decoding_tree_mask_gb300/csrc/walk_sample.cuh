@@ -1280,8 +1280,11 @@ __global__ void __launch_bounds__(kThreads, DK == DRAFT_POINT ? 2 : 1)
         cmd = lead<CL>(sm, sm.cmd);
         if (cmd == CMD_DONE || cmd == CMD_BONUS) break;
         if (LAZY && cmd == CMD_STATS) {
-            lazy_stats<DT, DK, DDT>(P, sm, base, sm.node,
-                                    reinterpret_cast<uint4 *>(subsum + lazy_ring_offset(P.V)));
+            // rows in host memory are read with plain loads: cp.async copies from host memory
+            // ran at half the rate over the host link (0.90 against 0.41 ms per large-tree call)
+            lazy_stats<DT, DK, DDT>(
+                P, sm, base, sm.node,
+                P.host_rows ? nullptr : reinterpret_cast<uint4 *>(subsum + lazy_ring_offset(P.V)));
             continue;
         }
         const Ctx c = node_ctx<DT, DK, DDT>(P, sm, base, sm.node);
