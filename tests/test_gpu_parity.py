@@ -245,6 +245,29 @@ def test_bonus_in_the_ragged_last_chunk(h, orc, dtype, V, lazy):
     assert (gpu["bonus"][ok] >= last).mean() > 0.3
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["greedy", "sample", "lazy"])
+def test_maximum_vocabulary(h, orc, dtype, mode):
+    """V = 2^21, the largest vocabulary a handle serves: 8192 sub-tile sums per row, bonus
+    chunks of 1024 sub-tiles (more than the register draw holds, so the chunk is summed and
+    searched), and the lazy walk's largest shared-memory request."""
+    V = 1 << 21
+    w = W.WORKLOADS["sampling_trie"].scaled(B=2, N=6, V=V, dtype=dtype, boost=10.0,
+                                            sigma=2.0, temperature=1.0, seed=21 + len(mode))
+    x = W.make(w, device=DEV)
+    if mode == "greedy":
+        got = PY.gpu_greedy(h, x["logits"], x["draft_token"], x["parent"])
+        PY.assert_exact(got, orc.verify_greedy(PY.host(x["logits"]), x["tok_np"],
+                                               x["parent_np"]))
+        return
+    fn = G.verify_sample_lazy if mode == "lazy" else G.verify_sample
+    gpu = PY.to_np(fn(h, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"]))
+    torch.cuda.synchronize()
+    ref = PY.oracle_sample(orc, x["logits"], x["draft_token"], x["parent"], 1.0, x["uniforms"])
+    PY.compare_sample(gpu, ref)
+    assert (gpu["status"] == 0).all()
+
+
 def test_sample_point_many_small_requests(h, orc):
     w = W.WORKLOADS["sampling_trie"].scaled(B=256, N=24, V=3001, dtype="f32", boost=6.0,
                                             sigma=1.5, temperature=1.0, seed=9)
