@@ -160,3 +160,49 @@ def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
     assert st.cpu().numpy().tolist() == ref_st.tolist() == [0] * B
     assert np.array_equal(gk.cpu().numpy(), ref_k)
     assert np.array_equal(gv.cpu().numpy(), ref_v)
+
+
+@pytest.mark.parametrize("cache,scale", [(K.SAME, None), (K.FP8_E4M3, 0.25),
+                                         (K.FP8_E5M2, 0.0173)])
+@pytest.mark.parametrize("B,H,D", [(1030, 2, 16), (4, 33, 128)])
+def test_kv_commit_many_requests_and_pieces(cache, scale, B, H, D):
+    """More requests than a CTA keeps in shared memory (1030 > 1024: the accepted length and
+    position of each unit's request are read from global memory instead), and slots of
+    33 x 128 = 4224 elements (two units each, 4096 + 128)."""
+    rng = np.random.default_rng(B + 7 * cache)
+    N, bs = 4, 8
+    al = rng.integers(0, N, B).astype(np.int32)           # chains: slots 0..al[b]
+    kv = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        kv[b, :al[b] + 1] = np.arange(al[b] + 1)
+    kv[B // 2] = -1                                       # a failed request
+    al[B // 2] = 0
+    table = rng.permutation(B).reshape(B, 1).astype(np.int32)
+    pos = rng.integers(0, bs - N + 1, B).astype(np.int32)
+    src = torch.from_numpy((rng.standard_normal((B, N, H, D)) * 2).astype(np.float32))
+    tk, tv = src.to(torch.bfloat16), (src * -0.5).to(torch.bfloat16)
+    kf, vf = tk.float().numpy(), tv.float().numpy()
+    shape = (B, bs, H, D)
+    if cache == K.SAME:
+        ck0 = torch.full(shape, 3.0, dtype=torch.bfloat16)
+        ref_k, ref_v, ref_st = K.kv_commit(kf, vf, kv, al, ck0.float().numpy(),
+                                           ck0.float().numpy(), K.NHD, bs, table, pos)
+    else:
+        ck0 = torch.full(shape, 0x33, dtype=torch.uint8)
+        ref_k, ref_v, ref_st = K.kv_commit(kf, vf, kv, al, ck0.numpy(), ck0.numpy(), K.NHD, bs,
+                                           table, pos, cache_kind=cache, k_scale=scale,
+                                           v_scale=scale)
+    with G.Handle(B, N, 1 << 10, 0) as hh:
+        gk, gv = ck0.to(DEV), ck0.clone().to(DEV)
+        st = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        sc = torch.tensor([scale], dtype=torch.float32, device=DEV) if scale else None
+        G.spec_kv_commit(hh, tk.to(DEV), tv.to(DEV), torch.from_numpy(kv).to(DEV),
+                         torch.from_numpy(al).to(DEV), gk, gv, K.NHD,
+                         torch.from_numpy(table).to(DEV), torch.from_numpy(pos).to(DEV),
+                         cache_kind=cache, k_scale=sc, v_scale=sc, commit_status=st)
+        torch.cuda.synchronize()
+    assert st.cpu().numpy().tolist() == ref_st.tolist() == [0] * B
+    got_k = gk.cpu().float().numpy() if cache == K.SAME else gk.cpu().numpy()
+    got_v = gv.cpu().float().numpy() if cache == K.SAME else gv.cpu().numpy()
+    assert np.array_equal(got_k, ref_k)
+    assert np.array_equal(got_v, ref_v)
