@@ -560,10 +560,33 @@ def test_host_argument_errors(h):
     with pytest.raises(G.SpecError) as e:
         G.Handle(4, 65, 100)
     assert e.value.code == G.SPEC_ERR_UNSUPPORTED
-    # B == 0 is a no-op
-    G.spec_verify_greedy(h, x["logits"][:0], x["draft_token"][:0], x["parent"][:0],
+    # B == 0 is a no-op for every call: nothing is launched or written
+    e = {k: x[k][:0] for k in ("logits", "draft_token", "parent", "uniforms")}
+    before = {k: v.clone() for k, v in out.items()}
+    G.spec_verify_greedy(h, e["logits"], e["draft_token"], e["parent"], out["accept_len"],
+                         out["out_tokens"], out["kv_commit"], out["bonus"], out["status"])
+    G.spec_verify_sample(h, e["logits"], e["draft_token"], e["parent"], 1.0, e["uniforms"],
                          out["accept_len"], out["out_tokens"], out["kv_commit"], out["bonus"],
                          out["status"])
+    G.spec_verify_greedy_lazy(h, e["logits"], e["draft_token"], e["parent"], out["accept_len"],
+                              out["out_tokens"], out["kv_commit"], out["bonus"], out["status"])
+    G.spec_verify_sample_lazy(h, e["logits"], e["draft_token"], e["parent"], 1.0, e["uniforms"],
+                              out["accept_len"], out["out_tokens"], out["kv_commit"],
+                              out["bonus"], out["status"])
+    # (empty views of allocated tensors, so that every pointer is a valid one)
+    mask = dict(anc=torch.zeros((1, 4), dtype=torch.int64, device=DEV)[:0],
+                depth=torch.zeros((1, 4), dtype=torch.int32, device=DEV)[:0],
+                status=torch.zeros(1, dtype=torch.int32, device=DEV)[:0])
+    G.spec_build_tree_mask(h, e["parent"], mask["anc"], mask["depth"], mask["status"])
+    kvsrc = torch.zeros((1, 4, 2, 16), dtype=torch.bfloat16, device=DEV)[:0]
+    cache = torch.zeros((2, 8, 2, 16), dtype=torch.bfloat16, device=DEV)
+    G.spec_kv_commit(h, kvsrc, kvsrc, e["parent"], out["accept_len"][:0], cache, cache.clone(),
+                     G.SPEC_KV_NHD, torch.zeros((1, 1), dtype=torch.int32, device=DEV)[:0],
+                     torch.zeros(1, dtype=torch.int32, device=DEV)[:0])
+    torch.cuda.synchronize()
+    for k, v in out.items():
+        assert torch.equal(v, before[k]), k
+    assert not cache.any()
 
 
 def test_side_stream_and_profiling(h):
