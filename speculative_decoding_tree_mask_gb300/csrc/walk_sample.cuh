@@ -49,8 +49,11 @@ namespace {
 #ifndef SPEC_DENSE_PASS_UNROLL
 #define SPEC_DENSE_PASS_UNROLL 4
 #endif
+// 16-byte loads in flight per thread in the lazy row pass's register loop: rows in host memory
+// (read over the host link: 0.403 ms per large-tree call with 4, 0.413 ms with 2) and rows that
+// are not 16-byte aligned.
 #ifndef SPEC_LAZY_UNROLL
-#define SPEC_LAZY_UNROLL 2   // 16-byte loads in flight per thread in the lazy row pass (rows that are not 16-byte aligned)
+#define SPEC_LAZY_UNROLL 4
 #endif
 // Lazy row passes over 16-byte aligned rows stage their loads through a ring of cp.async
 // copies in shared memory instead: SPEC_LAZY_RING vectors in flight per thread (32 KiB per
