@@ -111,25 +111,27 @@ __device__ __forceinline__ float fp8_quotient(float x, float s, float y, bool &o
 // The correctly rounded division, kept out of line: it runs for a few elements in a million.
 __device__ __noinline__ float div_rn(float x, float s) { return __fdiv_rn(x, s); }
 
-// The common case of fp8_quotient, cheaply: q1 (same steps) in the fp8 normal binades with its
-// dropped mantissa bits more than two steps from the midpoint pattern. Elements that fail this
-// test take fp8_quotient_full (zeros, the subnormal range, saturation, near-ties, exact
-// quotients, non-finite). Power-of-two scales, whose quotients are exact and land on fp8
-// midpoints often (one 16-bit source value in 16 for e4m3), never come here.
+// The common case, cheaper still: q0 = RN(x y) alone. With y = RN(1/s), x y = (x/s)(1 + e1)
+// and q0 = x y (1 + e2), |e1|, |e2| <= 2^-24, so q0 is within 2^-23 |x/s|, two steps of its own
+// binade, of x / s, and RN(x / s) within half a step more: within three steps of q0. So q0 in
+// the fp8 normal binades with its dropped mantissa bits more than three steps from the
+// midpoint pattern encodes like RN(x / s). Elements that fail this test take
+// fp8_quotient_full (zeros, the subnormal range, saturation, near-ties, exact quotients,
+// non-finite). Power-of-two scales, whose quotients are exact and land on fp8 midpoints often
+// (one 16-bit source value in 16 for e4m3), never come here.
 template <int CACHE>
-__device__ __forceinline__ float fp8_q1(float x, float s, float y) {
-    const float q0 = x * y;
-    return fmaf(fmaf(-q0, s, x), y, q0);
+__device__ __forceinline__ float fp8_q0(float x, float y) {
+    return x * y;
 }
 template <int CACHE>
-__device__ __forceinline__ bool fp8_fast_ok(float q1) {
+__device__ __forceinline__ bool fp8_fast_ok(float q0) {
     constexpr int KB = CACHE == 1 ? 3 : 2;
     constexpr int EMIN = CACHE == 1 ? -6 : -14;
     constexpr int EMAX = CACHE == 1 ? 8 : 15;
     constexpr uint32_t LO = uint32_t(127 + EMIN) << 23, RANGE = uint32_t(EMAX - EMIN + 1) << 23;
     constexpr uint32_t DROP = (1u << (23 - KB)) - 1u, HALF = 1u << (22 - KB);
-    const uint32_t mag = __float_as_uint(q1) & 0x7fffffffu;
-    return mag - LO < RANGE && (mag & DROP) - HALF + 2u > 4u;
+    const uint32_t mag = __float_as_uint(q0) & 0x7fffffffu;
+    return mag - LO < RANGE && (mag & DROP) - HALF + 3u > 6u;
 }
 template <int CACHE>
 __device__ __noinline__ float fp8_quotient_full(float x, float s, float y, bool fast) {
@@ -140,7 +142,7 @@ __device__ __noinline__ float fp8_quotient_full(float x, float s, float y, bool 
 
 // How a scale's quotients are formed: a power-of-two scale (its reciprocal exact, so
 // x * RN(1/s) is the same real number as x / s and rounds alike: one multiply, no test), a
-// scale with a normal reciprocal (fp8_q1 and fp8_fast_ok, then fp8_quotient_full), or the
+// scale with a normal reciprocal (fp8_q0 and fp8_fast_ok, then fp8_quotient_full), or the
 // correctly rounded division for every element.
 enum { Q_POW2 = 0, Q_RECIP = 1, Q_DIV = 2 };
 __device__ __forceinline__ int scale_mode(float s) {
@@ -216,14 +218,23 @@ __device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, f
         }
     }
     float q[8];
+    // clean: every quotient is finite and at least the smallest fp8 subnormal in magnitude, so
+    // its code is nonzero, the conversion keeps its sign, and no NaN or -0 needs fixing
+    bool clean = false;
     if (mode == Q_POW2) {
+        constexpr uint32_t LEAST = uint32_t(127 + (CACHE == 1 ? -9 : -16)) << 23;
+        unsigned odd = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = x[i] * rcp;
+        for (int i = 0; i < 8; ++i) {
+            q[i] = x[i] * rcp;
+            odd |= (__float_as_uint(q[i]) & 0x7fffffffu) - LEAST >= 0x7f800000u - LEAST;
+        }
+        clean = odd == 0u;
     } else {
         unsigned slow = mode == Q_RECIP ? 0u : 0xffu;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            q[i] = fp8_q1<CACHE>(x[i], scale, rcp);
+            q[i] = fp8_q0<CACHE>(x[i], rcp);
             slow |= fp8_fast_ok<CACHE>(q[i]) ? 0u : 1u << i;
         }
         if (slow) {
@@ -232,17 +243,21 @@ __device__ __forceinline__ void store8(const uint4 *raw, void *dst, size_t di, f
                 if (slow & (1u << i))
                     q[i] = fp8_quotient_full<CACHE>(x[i], scale, rcp, mode == Q_RECIP);
         }
+        clean = slow == 0u;
     }
-    // pairs (one conversion per two elements) with the signs OR'd in: the conversion gives +0
-    // for a negative value that rounds to zero, the format keeps -0
+    // pairs (one conversion per two elements); unless clean, the signs OR'd in (the conversion
+    // gives +0 for a negative value that rounds to zero, the format keeps -0) and NaN as 0x7F
     uint32_t c[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        c[i] = fp8x2(q[2 * i], q[2 * i + 1], CACHE) |
-               ((__float_as_uint(q[2 * i]) >> 24) & 0x80u) |
-               ((__float_as_uint(q[2 * i + 1]) >> 16) & 0x8000u);
-        if (q[2 * i] != q[2 * i]) c[i] = (c[i] & 0xff00u) | 0x7fu;           // NaN: 0x7F
-        if (q[2 * i + 1] != q[2 * i + 1]) c[i] = (c[i] & 0x00ffu) | 0x7f00u;
+    for (int i = 0; i < 4; ++i) c[i] = fp8x2(q[2 * i], q[2 * i + 1], CACHE);
+    if (!clean) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c[i] |= ((__float_as_uint(q[2 * i]) >> 24) & 0x80u) |
+                    ((__float_as_uint(q[2 * i + 1]) >> 16) & 0x8000u);
+            if (q[2 * i] != q[2 * i]) c[i] = (c[i] & 0xff00u) | 0x7fu;
+            if (q[2 * i + 1] != q[2 * i + 1]) c[i] = (c[i] & 0x00ffu) | 0x7f00u;
+        }
     }
     uint2 o;
     o.x = c[0] | (c[1] << 16);

@@ -114,8 +114,8 @@ def test_kv_commit_matches_oracle(h, src, cache, layout, D, scales):
 @pytest.mark.parametrize("cache", [K.FP8_E4M3, K.FP8_E5M2])
 def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
     """The fp8 encoding of x / scale near every fp8 rounding boundary: quotients placed on the
-    midpoints between adjacent fp8 values (ties to even), a few float32 steps either side of
-    them, beyond the largest finite value (saturation) and under the smallest subnormal (zero),
+    midpoints between adjacent fp8 values (ties to even), up to six float32 steps either side
+    of them (the library's shortcut defers within three), beyond the largest finite value (saturation) and under the smallest subnormal (zero),
     for scales that are powers of two (the quotients land on the midpoints exactly) and scales
     that are not. These are the cases where the library's reciprocal shortcut must defer to the
     correctly rounded division; the cache must equal the oracle's encoding bit for bit."""
@@ -128,7 +128,7 @@ def test_kv_commit_fp8_quotients_at_rounding_boundaries(h, cache):
     mids = np.concatenate([mids, least * np.array([0.3, 0.2, 0.126, 0.124, 0.1, 1e-3]),
                            [1e-30, 1e-40]])
     t = mids.astype(np.float32)
-    steps = (t.view(np.int32)[:, None] + np.arange(-3, 4, dtype=np.int32)[None, :]).ravel()
+    steps = (t.view(np.int32)[:, None] + np.arange(-6, 7, dtype=np.int32)[None, :]).ravel()
     t = steps.astype(np.int32).view(np.float32)
     t = np.concatenate([t, -t, np.float32([0.0, -0.0])])   # and zeros of both signs
     B, N, H, D = 4, 8, 2, 64
