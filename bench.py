@@ -649,7 +649,7 @@ def bench_ours(args):
 
     # f2 and f1 on their own workloads: the KV commit after a verify call, and the dense chain
     check = rank == 0 and not args.skip_parity
-    extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(h, dev, stream, args),
+    extra = {} if args.skip_extra else {"kv_commit": bench_kv_commit(dev, stream, args),
                                         "dense_chain": bench_dense_chain(dev, stream, args,
                                                                          check),
                                         "small_tries": bench_small_tries(dev, stream, args,
@@ -790,11 +790,18 @@ def _hbm(bytes_moved: int, ms: float) -> dict:
             "peak_source": kind}
 
 
-def bench_kv_commit(h, dev, stream, args):
+def bench_kv_commit(dev, stream, args):
     """KV commit of 8 slots per request (root + 7 accepted) for B=256, N=64, 32 heads x 128,
-    bf16 sources, into an NHD paged cache of 16-token blocks: bf16 and fp8 (e4m3) caches."""
+    bf16 sources, into an NHD paged cache of 16-token blocks: bf16 and fp8 (e4m3) caches. Its
+    own handle, sized for this workload whatever the verify legs' batch."""
     from speculative_decoding_tree_mask_gb300 import binding as G
     B, N, H, D, bs = 256, 64, 32, 128, 16
+    with G.Handle(B, N, 1 << 10, dev.index if dev.index is not None else 0) as h:
+        return _kv_commit_legs(h, dev, stream, B, N, H, D, bs)
+
+
+def _kv_commit_legs(h, dev, stream, B, N, H, D, bs):
+    from speculative_decoding_tree_mask_gb300 import binding as G
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     src_k = torch.randn((B, N, H, D), device=dev, generator=g).to(torch.bfloat16)
@@ -1054,15 +1061,13 @@ def bench_budget(h, x, w, dev, stream, args):
 
 def bench_leg(args):
     """One auxiliary leg on its own (for profiling runs): prints that leg's JSON."""
-    from speculative_decoding_tree_mask_gb300 import binding as G
     torch.cuda.set_device(0)
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev)
     legs = {"small_tries": lambda: bench_small_tries(dev, stream, args, not args.skip_parity),
             "dense_chain": lambda: bench_dense_chain(dev, stream, args, not args.skip_parity)}
     if args.leg == "kv_commit":
-        with G.Handle(256, 64, 1 << 10, 0) as h:
-            res = bench_kv_commit(h, dev, stream, args)
+        res = bench_kv_commit(dev, stream, args)
     else:
         res = legs[args.leg]()
     print(json.dumps({"leg": args.leg, **res}), flush=True)
